@@ -1,0 +1,410 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself:
+closed forms, brute force on tiny inputs, library routines on special cases
+and the numbers the pages print. CPU only."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ------------------------------------------------------------------ bf16 ---
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    # On values that are exact in fp32, torch's fp32 -> bf16 conversion is a
+    # single RNE rounding: the oracle must agree bit for bit.
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),   # subnormals
+        (rng.standard_normal(2000) * 3e38).astype(np.float32),    # near overflow
+        np.array([0.0, -0.0, 1.0, -1.0, 65504.0, 3.3895314e38, 1e-45], np.float32),
+    ])
+    # halfway points between neighbouring bf16 values, both parities
+    base = (rng.integers(0, 0x7F00, 3000).astype(np.uint32) << 16)
+    halfway = (base | 0x8000).view(np.float32)
+    vals = np.concatenate([vals, halfway, -halfway])
+    vals = vals[np.isfinite(vals)]
+    ours = O.f64_to_bf16_bits(vals.astype(np.float64))
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_round_is_single_rounding_from_double():
+    one = 1.0
+    cases = {
+        one + 2.0 ** -8: 1.0,                        # tie -> even (1.0)
+        one + 3 * 2.0 ** -8: one + 2.0 ** -6,        # tie -> even (upper)
+        one + 2.0 ** -8 + 2.0 ** -40: one + 2.0 ** -7,  # above the tie: up
+        -(one + 2.0 ** -8 + 2.0 ** -40): -(one + 2.0 ** -7),
+        2.0 ** 128: math.inf,
+        (2 - 2.0 ** -8) * 2.0 ** 127: math.inf,      # rounds up past the max
+        (2 - 2.0 ** -7) * 2.0 ** 127: (2 - 2.0 ** -7) * 2.0 ** 127,  # bf16 max
+        2.0 ** -133: 2.0 ** -133,                   # smallest subnormal
+        2.0 ** -134: 0.0,                           # tie -> even (zero)
+        1.5 * 2.0 ** -134: 2.0 ** -133,
+    }
+    for v, want in cases.items():
+        got = O.bf16_round(np.array([v]))[0]
+        assert got == want, (v, got, want)
+
+
+def test_bf16_bits_roundtrip():
+    bits = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = O.bf16_bits_to_f64(bits)
+    fin = np.isfinite(vals)
+    back = O.f64_to_bf16_bits(vals[fin])
+    # -0.0 and 0.0 keep their sign; every finite pattern maps to itself
+    assert np.array_equal(back, bits[fin])
+
+
+# ---------------------------------------------------------------- router ---
+
+def test_router_logits_match_library_matmul():
+    x = O.bf16_round(rng.standard_normal((37, 64)))
+    g = O.bf16_round(rng.standard_normal((64, 5)) / 8)
+    b = rng.standard_normal(5).astype(np.float32)
+    ref = torch.matmul(torch.from_numpy(x), torch.from_numpy(g)).to(torch.float32) + torch.from_numpy(b)
+    assert np.array_equal(O.router_logits(x, g, b), ref.numpy())
+
+
+def _topk_brute(row, k):
+    # the k-subset whose keys (logit, -index), sorted descending, form the
+    # lexicographically largest tuple; then its members in that order
+    E = len(row)
+    key = lambda e: (float(row[e]), -e)
+    best = None
+    for S in itertools.combinations(range(E), k):
+        ks = sorted((key(e) for e in S), reverse=True)
+        if best is None or ks > best[0]:
+            best = (ks, S)
+    return [-kk[1] for kk in best[0]]
+
+
+@pytest.mark.parametrize("kind", ["normal", "binary", "few_levels"])
+def test_topk_brute_force(kind):
+    for trial in range(40):
+        T = int(rng.integers(1, 65))
+        E = int(rng.integers(1, 9))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        if kind == "normal":
+            lg = rng.standard_normal((T, E)).astype(np.float32)
+        elif kind == "binary":
+            lg = rng.integers(0, 2, (T, E)).astype(np.float32)
+        else:
+            lg = (rng.integers(-2, 3, (T, E)) * 0.5).astype(np.float32)
+        idx = O.topk(lg, k)
+        for t in range(T):
+            assert list(idx[t]) == _topk_brute(lg[t], k)
+
+
+def test_topk_equal_logits_lowest_indices_first():
+    lg = np.zeros((3, 7), np.float32)
+    assert (O.topk(lg, 4) == np.arange(4)).all()
+
+
+def test_softmax_closed_forms():
+    E = 6
+    p = O.softmax(np.zeros((2, E), np.float32))
+    assert np.allclose(p, 1.0 / E, rtol=0, atol=1e-15)
+    L = 2.5
+    lg = np.zeros((1, E), np.float32)
+    lg[0, 3] = L
+    p = O.softmax(lg)
+    assert math.isclose(p[0, 3], math.exp(L) / (math.exp(L) + E - 1), rel_tol=1e-14)
+    for k in (1, 2, 4):
+        r = O.route_from_logits(lg, k)
+        assert r.idx[0, 0] == 3
+        assert math.isclose(r.w[0, 0], math.exp(L) / (math.exp(L) + k - 1), rel_tol=1e-14)
+
+
+def test_renormalised_weights():
+    lg = rng.standard_normal((50, 9)).astype(np.float32)
+    for k in range(1, 10):
+        r = O.route_from_logits(lg, k)
+        assert np.allclose(r.w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert (np.diff(r.w, axis=1) <= 0).all()          # sorted like the logits
+        if k == 1:
+            assert (r.w == 1.0).all()
+        if k == 9:
+            assert np.allclose(np.take_along_axis(r.p, r.idx.astype(np.int64), 1), r.w, atol=1e-15)
+
+
+def test_nonfinite_logits_rejected():
+    lg = np.zeros((2, 4), np.float32)
+    lg[1, 2] = np.nan
+    with pytest.raises(ValueError):
+        O.softmax(lg)
+
+
+# ------------------------------------------------------------------- aux ---
+
+@pytest.mark.parametrize("T,E,k", [(16, 4, 1), (30, 8, 2), (64, 64, 6), (5, 3, 3)])
+def test_aux_is_one_for_uniform_logits(T, E, k):
+    lg = np.zeros((T, E), np.float32)
+    r = O.route_from_logits(lg, k)
+    st = O.load_balance_stats(r.idx, r.p, E)
+    # every token picks experts 0..k-1: f_e = 1/k there, P_e = 1/E
+    assert np.allclose(st.f[:k], 1.0 / k) and (st.f[k:] == 0).all()
+    assert math.isclose(st.aux, 1.0, rel_tol=1e-13)
+
+
+def test_aux_is_one_when_either_distribution_is_uniform():
+    E, k = 8, 2
+    # balanced assignments (uniform f) with arbitrary router probabilities
+    idx = np.array([[e, (e + 1) % E] for e in range(E)] * 5, np.int32)
+    p = rng.dirichlet(np.ones(E), size=idx.shape[0])
+    st = O.load_balance_stats(idx, p, E)
+    assert np.allclose(st.f, 1.0 / E)
+    assert math.isclose(st.aux, 1.0, rel_tol=1e-13)
+    # skewed assignments with uniform probabilities
+    idx2 = np.array([[0, 1]] * 30 + [[2, 5]] * 3, np.int32)
+    st2 = O.load_balance_stats(idx2, np.full((33, E), 1.0 / E), E)
+    assert math.isclose(st2.aux, 1.0, rel_tol=1e-13)
+    assert math.isclose(st2.f.sum(), 1.0, rel_tol=1e-15)
+
+
+def test_aux_above_one_when_mass_and_traffic_coincide():
+    # all tokens send both slots to experts 0,1 and put most probability
+    # there: aux = E * (1/2 * P0 + 1/2 * P1) with P0 = P1 = 0.45
+    E = 10
+    idx = np.tile(np.array([[0, 1]], np.int32), (20, 1))
+    p = np.full((20, E), 0.1 / 8)
+    p[:, 0] = p[:, 1] = 0.45
+    st = O.load_balance_stats(idx, p, E)
+    assert math.isclose(st.aux, E * 0.45, rel_tol=1e-13)
+
+
+# ------------------------------------------------------ capacity / drop ----
+
+def test_capacity_of_named_workloads():
+    # hand evaluation of max(1, ceil(cf*T*k/E)):
+    #   1.25*1024/8 = 160, 1.0*8192/16 = 512, 1.25*65536/8 = 10240,
+    #   1.25*98304/64 = 1920, 1.1*262144/128 = 2252.8 -> 2253 (floor: 2252)
+    assert O.capacity(512, 8, 2, 1.25) == 160
+    assert O.capacity(4096, 16, 2, 1.0) == 512
+    assert O.capacity(32768, 8, 2, 1.25) == 10240
+    assert O.capacity(16384, 64, 6, 1.25) == 1920
+    assert O.capacity(131072, 128, 2, 1.1) == 2253
+    assert O.capacity(1, 256, 1, 0.01) == 1
+    assert O.capacity(0, 4, 2, 1.0) == 1
+
+
+def _dispatch_brute(idx, E, C):
+    T, k = idx.shape
+    seen = [0] * E
+    pos = np.zeros((T, k), np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            pos[t, j] = seen[e]
+            seen[e] += 1
+    kept = pos < C
+    kept_counts = np.array([min(s, C) for s in seen])
+    off = [0]
+    for e in range(E):
+        off.append(off[-1] + int(kept_counts[e]))
+    dest = np.full((T, k), -1, np.int64)
+    for t in range(T):
+        for j in range(k):
+            if kept[t, j]:
+                dest[t, j] = off[int(idx[t, j])] + pos[t, j]
+    return pos, kept_counts, np.array(off), dest
+
+
+def _random_idx(T, E, k, skew=0.0):
+    pr = np.exp(-skew * np.arange(E))
+    pr /= pr.sum()
+    return np.stack([rng.choice(E, size=k, replace=False, p=pr) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k,cf,skew", [
+    (1, 1, 1, 1.0, 0), (7, 3, 2, 0.5, 0), (64, 8, 2, 1.25, 0.0), (64, 8, 2, 0.6, 0.7),
+    (200, 16, 3, 1.0, 0.3), (50, 5, 5, 1.0, 0), (300, 12, 4, 0.2, 0.1)])
+def test_dispatch_matches_sequential_simulation(T, E, k, cf, skew):
+    idx = _random_idx(T, E, k, skew)
+    C = O.capacity(T, E, k, cf)
+    d = O.dispatch_plan(idx, E, C)
+    pos, kc, off, dest = _dispatch_brute(idx, E, C)
+    assert np.array_equal(d.pos, pos)
+    assert np.array_equal(d.kept_counts, kc)
+    assert np.array_equal(d.offsets, off)
+    assert np.array_equal(d.dest_row, dest)
+    # counts: sum routed = T*k, sum kept = T*k - drops
+    routed = np.bincount(idx.reshape(-1), minlength=E)
+    assert routed.sum() == T * k
+    drops = int((d.dest_row < 0).sum())
+    assert d.kept_counts.sum() == T * k - drops == d.N
+    # bijection onto [0, N), inverse map, (expert, token) order of rows
+    rows = d.dest_row[d.dest_row >= 0]
+    assert np.array_equal(np.sort(rows), np.arange(d.N))
+    tt, jj = np.nonzero(d.dest_row >= 0)
+    assert np.array_equal(d.src_token[d.dest_row[tt, jj]], tt)
+    ek = np.array([(int(idx[t, j]), int(t)) for t, j in zip(tt, jj)])
+    by_row = ek[np.argsort(d.dest_row[tt, jj])]
+    assert all(tuple(by_row[i]) < tuple(by_row[i + 1]) for i in range(len(by_row) - 1))
+
+
+def test_dispatch_hand_example():
+    # 6 tokens, 4 experts, top-2, cf = 0.75 -> C = ceil(0.75*12/4) = 3
+    idx = np.array([[0, 1], [1, 0], [2, 0], [0, 3], [1, 2], [3, 1]], np.int32)
+    C = O.capacity(6, 4, 2, 0.75)
+    assert C == 3
+    d = O.dispatch_plan(idx, 4, C)
+    # expert 0 is chosen by tokens 0,1,2,3 -> token 3 dropped; expert 1 by
+    # 0,1,4,5 -> token 5 dropped; expert 2 by 2,4; expert 3 by 3,5
+    assert list(d.kept_counts) == [3, 3, 2, 2]
+    assert list(d.offsets) == [0, 3, 6, 8, 10]
+    assert d.dest_row.tolist() == [[0, 3], [4, 1], [6, 2], [-1, 8], [5, 7], [9, -1]]
+    assert d.src_token.tolist() == [0, 1, 2, 0, 1, 4, 2, 4, 3, 5]
+
+
+def test_uniform_logits_drop_every_late_token():
+    T, E, k, H = 40, 4, 2, 8
+    cf = 0.5                                    # C = ceil(0.5*80/4) = 10
+    x = O.bf16_round(rng.standard_normal((T, H)))
+    gate = np.zeros((H, E))
+    W1 = O.bf16_round(rng.standard_normal((E, H, 16)) * 0.3)
+    W2 = O.bf16_round(rng.standard_normal((E, 16, H)) * 0.3)
+    out = O.layer_forward(x, gate, None, W1, W2, k, cf)
+    C = out.dispatch.C
+    assert C == 10
+    assert (out.routing.idx == np.arange(k)).all()
+    assert (out.dispatch.dest_row[:C] >= 0).all()
+    assert (out.dispatch.dest_row[C:] == -1).all()
+    assert (out.y[C:] == 0).all()
+    assert list(out.dispatch.kept_counts) == [C, C, 0, 0]
+
+
+# ------------------------------------------------------------------- FFN ---
+
+def test_gelu_tanh_matches_library():
+    u = np.concatenate([rng.standard_normal(5000) * 4, [0.0, -30.0, 30.0]])
+    ref = torch.nn.functional.gelu(torch.from_numpy(u), approximate="tanh").numpy()
+    assert np.allclose(O.gelu_tanh(u), ref, rtol=1e-15, atol=1e-15)
+    v = rng.standard_normal(100)
+    assert np.allclose(O.gelu_tanh(v) - O.gelu_tanh(-v), v, atol=1e-14)
+
+
+def _torch_bf16(t64):
+    return t64.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+
+def test_single_expert_layer_is_a_dense_ffn():
+    # E = 1, k = 1, cf >= 1: nothing is dropped, every weight is 1, and the
+    # layer is the dense FFN x -> gelu(x W1) W2 with the same rounding points.
+    T, H, h = 33, 64, 96
+    x = O.bf16_round(rng.standard_normal((T, H)))
+    gate = O.bf16_round(rng.standard_normal((H, 1)))
+    W1 = O.bf16_round(rng.standard_normal((1, H, h)) / 8)
+    W2 = O.bf16_round(rng.standard_normal((1, h, H)) / 10)
+    out = O.layer_forward(x, gate, None, W1, W2, 1, 1.0)
+    xt, w1, w2 = (torch.from_numpy(a) for a in (x, W1[0], W2[0]))
+    act = _torch_bf16(torch.nn.functional.gelu(xt @ w1, approximate="tanh"))
+    ref = _torch_bf16(act @ w2).numpy()
+    # both sides round act and y to bf16; a matmul summed in another order
+    # can flip an act rounding, which moves y by a few bf16 ulps at most
+    assert np.allclose(out.y, ref, rtol=2.0 ** -5, atol=1e-3 * np.abs(ref).max())
+    assert np.mean(out.y == ref) > 0.95
+    assert (out.routing.w == 1).all() and (out.dispatch.dest_row >= 0).all()
+
+
+def test_all_experts_layer_is_a_soft_mixture():
+    # k = E and cf >= 1: every token visits every expert, so
+    # y = sum_e p_e FFN_e(x) with p the full softmax.
+    T, H, E, h = 20, 64, 3, 64
+    x = O.bf16_round(rng.standard_normal((T, H)))
+    gate = O.bf16_round(rng.standard_normal((H, E)) / 8)
+    W1 = O.bf16_round(rng.standard_normal((E, H, h)) / 8)
+    W2 = O.bf16_round(rng.standard_normal((E, h, H)) / 8)
+    out = O.layer_forward(x, gate, None, W1, W2, E, 1.0)
+    xt = torch.from_numpy(x)
+    lg = (xt @ torch.from_numpy(gate)).to(torch.float32).to(torch.float64)
+    p = torch.softmax(lg, dim=1)
+    acc = torch.zeros((T, H), dtype=torch.float64)
+    for e in range(E):
+        act = _torch_bf16(torch.nn.functional.gelu(xt @ torch.from_numpy(W1[e]), approximate="tanh"))
+        acc += p[:, e:e + 1] * _torch_bf16(act @ torch.from_numpy(W2[e]))
+    ref = _torch_bf16(acc).numpy()
+    assert np.allclose(out.y, ref, rtol=2.0 ** -5, atol=1e-3 * np.abs(ref).max())
+    assert np.mean(out.y == ref) > 0.9
+
+
+def test_token_outputs_equal_layer_rows():
+    T, H, E, k, h = 60, 64, 6, 2, 64
+    x = O.bf16_round(rng.standard_normal((T, H)))
+    gate = O.bf16_round(rng.standard_normal((H, E)) / 8)
+    W1 = O.bf16_round(rng.standard_normal((E, H, h)) / 8)
+    W2 = O.bf16_round(rng.standard_normal((E, h, H)) / 8)
+    out = O.layer_forward(x, gate, None, W1, W2, k, 0.8)
+    rows = np.array([0, 5, 17, 44, 59])
+    kept = out.dispatch.dest_row[rows] >= 0
+    y = O.token_outputs(x[rows], out.routing.idx[rows], out.routing.w[rows], kept, W1, W2)
+    assert np.array_equal(y, out.y[rows])
+
+
+# ------------------------------------------------------------ accounting ---
+
+def test_worked_example_accounting():
+    with open(os.path.join(GOLDEN, "worked_example_comm_bottleneck_2_2.json")) as f:
+        g = json.load(f)
+    i, n = g["inputs"], g["as_numbers"]
+    B = i["seq_len"] * i["micro_batch"]
+    assert B == n["tokens_B"]
+    assert O.dispatch_bytes(B, i["top_k"], i["H"], i["dtype_bytes"]) == n["dispatch_bytes_per_layer"]
+    fte = O.ffn_flops_per_token_expert(i["H"], i["h_exp"])
+    assert abs(fte - n["flop_per_token_expert_approx"]) / fte < 0.01
+    assert abs(2 * fte - n["flop_per_token_top2_approx"]) / fte < 0.02
+    layer = B * i["top_k"] * fte
+    assert abs(layer - n["flop_per_layer_approx"]) / layer < 0.03
+    a2a = 2 * O.dispatch_bytes(B, i["top_k"], i["H"], i["dtype_bytes"]) * i["moe_layers"]
+    assert abs(a2a - n["a2a_bytes_32_layers_approx"]) / a2a < 0.08
+    assert abs(O.comm_compute_ratio(14336, 2) - n["comm_compute_ratio_h14336_approx"]) < 0.05e-5
+    assert abs(O.comm_compute_ratio(2048, 2) - n["comm_compute_ratio_h2048_approx"]) < 0.05e-4
+
+
+# ------------------------------------- planted mistakes must trip a pin ----
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Each plausible slip in the oracle makes at least one pin fail."""
+    # floor instead of ceil in the capacity
+    monkeypatch.setattr(O, "capacity", lambda T, E, k, cf: max(1, int(cf * T * k / E)))
+    with pytest.raises(AssertionError):
+        test_capacity_of_named_workloads()
+    monkeypatch.undo()
+    # f normalised by T instead of T*k
+    real = O.load_balance_stats
+
+    def by_T(idx, p, E):
+        s = real(idx, p, E)
+        s.aux *= idx.shape[1]
+        return s
+    monkeypatch.setattr(O, "load_balance_stats", by_T)
+    with pytest.raises(AssertionError):
+        test_aux_is_one_for_uniform_logits(30, 8, 2)
+    monkeypatch.undo()
+    # ties broken toward the higher index
+    monkeypatch.setattr(O, "topk", lambda lg, k: (lg.shape[1] - 1 - np.argsort(
+        -np.asarray(lg)[:, ::-1], axis=1, kind="stable")[:, :k]).astype(np.int32))
+    with pytest.raises(AssertionError):
+        test_topk_brute_force("binary")
+    monkeypatch.undo()
+    # slot-major ("all first choices first") drop priority
+    def slot_major(idx, E, C):
+        T, k = idx.shape
+        d = real_plan(idx.T.copy(), E, C)
+        d.dest_row = d.dest_row.T.copy()
+        d.pos = d.pos.T.copy()
+        return d
+    real_plan = O.dispatch_plan
+    monkeypatch.setattr(O, "dispatch_plan", slot_major)
+    with pytest.raises(AssertionError):
+        test_dispatch_hand_example()
+    monkeypatch.undo()
