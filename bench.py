@@ -1,0 +1,349 @@
+"""Throughput of the MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one whole layer forward (router GEMM + softmax/top-k + stats,
+scan, permute, expert FFN GEMM1 + GELU, GEMM2, combine) over one batch of
+the workload, inputs resident in HBM. Every rank runs an independent
+replica on its own GPU (the layer needs no exchange for its output), the
+timed region is bracketed by a barrier and a device synchronisation, and
+rank 0 prints one JSON line with the max-over-ranks time.
+
+`--impl reference` times the CPU oracle as it stands on this host's cores
+on a bounded token sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s; grouped-GEMM TFLOP/s & permute GB/s vs GB300 peaks"
+DEFAULT_WORKLOAD = "large_expert"
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------ accounting ----
+
+def algorithmic_work(w: W.Workload, n_kept: int, n_tokens_any: int) -> dict:
+    """What each stage must move or compute (not what it happens to move):
+    router reads x and the gate and writes indices/weights; permute reads
+    each token row that has a kept slot once and writes each kept row once
+    (dispatch bytes of the comm bottleneck page, section 2.1, with drops
+    removed); GEMM1/GEMM2 are 2*N*H*h FLOP each (4*H*h per token-expert,
+    section 2.2); combine reads each kept row and writes each token row."""
+    T, H, E, k, h = w.T, w.H, w.E, w.k, w.h
+    return {
+        "route_bytes": 2 * T * H + 2 * H * E + 8 * T * k,
+        "route_flop": 2 * T * H * E,
+        "permute_bytes": 2 * H * (n_tokens_any + n_kept),
+        "gemm1_flop": 2 * n_kept * H * h,
+        "gemm2_flop": 2 * n_kept * h * H,
+        "combine_bytes": 2 * H * (n_kept + T),
+    }
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- our arm ----
+
+def run_ours(args, rank, world, local_rank):
+    import top_routing_expert_gb300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    moe.build()
+    moe.load_library()
+    w = W.get(args.workload)
+    inp = W.make_inputs(w, seed=rank)
+    s = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
+    ws = moe.Workspace(s, device=dev)
+    d = {kk: (v.to(dev) if v is not None else None) for kk, v in inp.items()}
+    T, E, k = w.T, w.E, w.k
+    y = torch.empty((T, w.H), dtype=torch.bfloat16, device=dev)
+    aux = torch.zeros(1, dtype=torch.float32, device=dev)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+    dest = torch.zeros((T, k), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux,
+                          offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
+                          stream=stream, events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # per-stage events, recorded once so that their handles exist
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.LAYER_NUM_EVENTS)]
+          for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    stage_ms = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j in range(moe.LAYER_NUM_EVENTS - 1)]
+    st = int(status.item())
+    n_kept = int(offsets[E].item())
+    any_kept = int((dest >= 0).any(dim=1).sum().item())
+
+    # end to end through the public API with host buffers: copy x in, read y
+    # and aux out, every step, inside the timed region
+    x_host = inp["x"].pin_memory()
+    y_host = torch.empty((T, w.H), dtype=torch.bfloat16).pin_memory()
+    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(d["x"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_fwd(s, x_dev, d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux, ws=ws,
+                          stream=stream)
+        y_host.copy_(y, non_blocking=True)
+        aux_host.copy_(aux, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        return None
+    pk = peaks()
+    work = algorithmic_work(w, n_kept, any_kept)
+    names = ["route", "scan", "permute", "gemm1", "gemm2", "combine"]
+    stage = dict(zip(names, stage_ms))
+    kern = {}
+    for nm, key, unit in [("route", "route_bytes", "GB/s"), ("permute", "permute_bytes", "GB/s"),
+                          ("combine", "combine_bytes", "GB/s"), ("gemm1", "gemm1_flop", "TFLOP/s"),
+                          ("gemm2", "gemm2_flop", "TFLOP/s")]:
+        sec = stage[nm] / 1e3
+        if unit == "GB/s":
+            a = work[key] / sec / 1e9
+            kern[nm] = {"ms": round(stage[nm], 4), "achieved": round(a, 1), "unit": unit,
+                        "frac_of_measured_hbm": round(a / pk["hbm_gbs"], 3)}
+        else:
+            a = work[key] / sec / 1e12
+            kern[nm] = {"ms": round(stage[nm], 4), "achieved": round(a, 1), "unit": unit,
+                        "frac_of_measured_bf16": round(a / pk["bf16_tflops"], 3)}
+    kern["scan"] = {"ms": round(stage["scan"], 4)}
+    gemm_ms = stage["gemm1"] + stage["gemm2"]
+    gemm_tf = (work["gemm1_flop"] + work["gemm2_flop"]) / (gemm_ms / 1e3) / 1e12
+    roofline = {"kernel": "grouped_gemm_kernel (expert FFN GEMM1+GELU and GEMM2)",
+                "bound": "tensor", "achieved": round(gemm_tf, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(gemm_tf / pk["bf16_tflops"], 4),
+                "peak_kind": f"{pk['source']} bf16 burst", "traffic": None}
+    tokens = T * world
+    line = {
+        "metric": METRIC, "value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**w.describe(), "parallelism": f"replicas x{world} (no exchange)",
+                   "l2": "inputs larger than L2 (x 268 MB, W1/W2 1.9 GB each); no flush"},
+        "clocks": clk,
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": T * w.H * 2,
+                "d2h_bytes_per_step": T * w.H * 2 + 4},
+        "gpu_launches": 7 * args.steps,
+        "roofline": roofline,
+        "kernels": kern,
+        "routing": {"kept_rows": n_kept, "assignments": T * k, "dropped": T * k - n_kept,
+                    "dev_status": st},
+    }
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens, inp)
+    return line
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def cpu_baseline(w: W.Workload, n_tokens: int, inp: dict) -> dict:
+    """The oracle as it stands, one layer forward of a bounded token sample of
+    the workload (its own capacity on the sample), timed on this host."""
+    import numpy as np
+    from oracle import moe_oracle as O
+
+    n = min(n_tokens, w.T)
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    x = f64(inp["x"][:n])
+    gate = f64(inp["gate"])
+    bias = None if inp["bias"] is None else inp["bias"].numpy()
+
+    class Lazy:
+        def __init__(self, t):
+            self.t = t
+
+        def __getitem__(self, e):
+            return f64(self.t[int(e)])
+
+    t0 = time.perf_counter()
+    O.layer_forward(x, gate, bias, Lazy(inp["W1"]), Lazy(inp["W2"]), w.k, w.cf)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"one oracle layer forward of the first {n} of {w.T} tokens "
+                      f"(float64 numpy, capacity from the sample's own T)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.get(args.workload)
+    # every step is one bounded oracle sample; keep the whole run short
+    n = max(16, args.cpu_tokens // max(1, args.steps + args.warmup))
+    inp = W.make_inputs(w, seed=0)
+    for _ in range(args.warmup):
+        cpu_baseline(w, n, inp)
+    vals = [cpu_baseline(w, n, inp) for _ in range(args.steps)]
+    secs = sum(v["seconds"] for v in vals)
+    value = n * args.steps / secs
+    cb = dict(vals[-1])
+    cb["value"] = round(value, 2)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "parallelism": "host cores"},
+        "cpu_baseline": cb,
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

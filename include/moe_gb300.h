@@ -1,0 +1,180 @@
+/*
+ * moe_gb300.h - C ABI of a GB300 (sm_103a) forward pass of one
+ * Mixture-of-Experts layer on one GPU.
+ *
+ * The layer (MoE comm bottleneck page, section 1.1; MoE module notes page,
+ * sections 3.1-3.3 and the MoELayer listing of 4.2):
+ *   logits  = x . gate (+ bias)                       router, a Linear H -> E
+ *   p       = softmax(logits) over the E experts
+ *   idx, w  = top-k of the logits, weights p renormalised over the k chosen
+ *   stats   = routed counts, P_e = mean_t p[t,e], aux = E * sum_e f_e P_e
+ *   dispatch: capacity C = max(1, ceil(cf * T*k / E)); each expert serves
+ *             its assignments in token order and drops those at position
+ *             >= C; kept rows are gathered expert-major into x_perm
+ *   FFN     : act = bf16(gelu_tanh(x_perm . W1[e])); y_perm = bf16(act . W2[e])
+ *   combine : y[t] = bf16(sum over kept slots j, ascending, of w[t,j] y_perm[row])
+ *
+ * Conventions for every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     shape struct is a host pointer. The caller owns all memory. The library
+ *     never allocates; scratch comes from the caller's workspace `ws`
+ *     (size from moe_workspace_size). Pointers must be 16-byte aligned.
+ *   - Arrays are dense and row-major: x [T,H], gate [H,E], W1 [E,H,h],
+ *     W2 [E,h,H], topk_idx/topk_w/dest_row [T,k], x_perm/y_perm [T*k,H],
+ *     act [T*k,h], y [T,H]. bf16 arrays hold raw bf16 bit patterns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise with the host. The number of
+ *     kept rows N is only known on the device, so row buffers hold T*k rows;
+ *     rows at index >= offsets[E] are left unspecified.
+ *   - Host-side checks return a status before anything is launched. A
+ *     launch failure returns MOE_ERR_CUDA. Problems found in device data
+ *     (bad expert index, non-finite logits, a wait that ran out) are OR-ed
+ *     as MOE_DEV_* bits into *dev_status; the kernels then finish normally.
+ *     The caller clears *dev_status; a NULL dev_status uses a workspace word.
+ *   - Workspace contents do not survive between calls, and two calls that
+ *     share a workspace must be ordered on one stream.
+ *   - Supported: 0 <= T, T*k < 2^31; 1 <= E <= 256; 1 <= k <= min(E, 8);
+ *     H and h multiples of 64, >= 64; capacity_factor finite and > 0.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_GB300_ABI_VERSION 1
+
+typedef uint16_t moe_bf16; /* a bf16 value as its 16 bits */
+
+typedef struct {
+  int64_t T;               /* tokens */
+  int64_t H;               /* hidden size */
+  int64_t E;               /* number of experts */
+  int64_t top_k;           /* experts per token, k */
+  int64_t h;               /* expert FFN width */
+  double capacity_factor;  /* cf, binary64 (see moe_capacity) */
+} moe_shape;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,        /* a required pointer is NULL */
+  MOE_ERR_SHAPE = 2,       /* a size is negative, zero where it may not be, or overflows */
+  MOE_ERR_UNSUPPORTED = 3, /* valid but outside the supported ranges above */
+  MOE_ERR_WORKSPACE = 4,   /* ws_bytes < moe_workspace_size */
+  MOE_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
+  MOE_ERR_CUDA = 6         /* a CUDA call or launch failed */
+} moe_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define MOE_DEV_BAD_INDEX 1u  /* an expert index outside [0,E): slot dropped */
+#define MOE_DEV_DUP_INDEX 2u  /* a token names one expert twice: later slot dropped */
+#define MOE_DEV_NONFINITE 4u  /* a router logit is NaN or infinite */
+#define MOE_DEV_TIMEOUT 8u    /* a pipeline wait gave up; outputs are incomplete */
+
+/* Number of CUDA events moe_layer_fwd records when given an event array. */
+#define MOE_LAYER_NUM_EVENTS 7
+
+/* Capacity per expert, C = max(1, ceil(cf * (T*k) / E)), evaluated in
+ * binary64 in exactly that order (MoE comm bottleneck, section 3.1, gives
+ * capacity = ceil(capacity_factor * tokens / num_experts); the MoE module
+ * notes' listing, section 4.2, counts tokens as T*k and floors C at 1).
+ * Returns -1 for E < 1, k < 1, T < 0 or a non-finite/non-positive cf.
+ * Host only; needs no GPU. */
+int64_t moe_capacity(int64_t T, int64_t E, int64_t top_k, double capacity_factor);
+
+/* Bytes of device workspace any entry point needs for this shape (one size
+ * serves all of them). Host only. Returns MOE_ERR_NULL / _SHAPE /
+ * _UNSUPPORTED for bad arguments. */
+moe_status moe_workspace_size(const moe_shape* s, size_t* bytes);
+
+/* Static text for a status code. Host only. */
+const char* moe_status_str(moe_status st);
+
+/* MOE_GB300_ABI_VERSION of the built library. Host only. */
+int moe_abi_version(void);
+
+/* Router: logits GEMM on the tensor cores, softmax, top-k, renormalised
+ * weights and the load-balancing statistics (MoE module notes, section 3.1
+ * router listing; MoE comm bottleneck, section 3.2 auxiliary loss).
+ *   in : x [T,H] bf16, gate [H,E] bf16, gate_bias [E] fp32 or NULL
+ *   out: topk_idx [T,k] int32 (largest logit first; equal logits by lower
+ *        expert index), topk_w [T,k] fp32 (sum to 1 per token),
+ *        routed_counts [E] int32 (assignments per expert before drops),
+ *        P [E] fp32 (mean softmax probability), aux [1] fp32
+ *        (E * sum_e routed_e/(T*k) * P_e; the loss weight alpha is the
+ *        caller's), logits_out [T,E] fp32 or NULL (bias included).
+ * routed_counts, P, aux may be NULL. */
+moe_status moe_route(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                     const float* gate_bias, int32_t* topk_idx, float* topk_w,
+                     int32_t* routed_counts, float* P, float* aux, float* logits_out,
+                     uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* The router's steps after the GEMM, on caller-given fp32 logits [T,E]
+ * (the MoE module notes, section 5.2, take top-k directly on the logits at
+ * inference). Same outputs and rules as moe_route; with equal logits the
+ * two give identical indices, weights and statistics. */
+moe_status moe_route_logits(const moe_shape* s, const float* logits, int32_t* topk_idx,
+                            float* topk_w, int32_t* routed_counts, float* P, float* aux,
+                            uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch: capacity-bounded, token-ordered permutation of token rows into
+ * expert-major order - the single-GPU form of the dispatch all-to-all (MoE
+ * comm bottleneck, sections 1.1 and 3.1: tokens beyond an expert's
+ * capacity are dropped, later tokens first).
+ *   in : x [T,H] bf16, topk_idx [T,k] int32
+ *   out: kept_counts [E] = min(routed_e, C); offsets [E+1] exclusive scan;
+ *        dest_row [T,k] = offsets[e] + position, or -1 if dropped;
+ *        src_token [T*k] (row -> token, rows < offsets[E]);
+ *        x_perm [T*k,H] bf16 (row dest_row[t,j] = x[t]).
+ * kept_counts, src_token may be NULL. Bad or repeated indices set
+ * MOE_DEV_BAD_INDEX / MOE_DEV_DUP_INDEX and that slot is dropped. */
+moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+                       int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                       int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Expert FFN over the ragged expert-major rows as two grouped GEMMs on the
+ * tensor cores (MoE comm bottleneck, section 5.1 grouped GEMM; expert =
+ * Linear -> GELU -> Linear, MoE module notes section 3.3, bias-free weights
+ * as in the 4.2 listing). Rows [offsets[e], offsets[e+1]) use expert e.
+ *   in : x_perm [T*k,H] bf16, offsets [E+1] int32, W1 [E,H,h], W2 [E,h,H]
+ *   out: act [T*k,h] bf16 = bf16(gelu_tanh(x_perm . W1[e])) (fp32 accumulate),
+ *        y_perm [T*k,H] bf16 = bf16(act . W2[e]). */
+moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int32_t* offsets,
+                          const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
+                          moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Combine: weighted sum of each token's kept expert rows, back at the
+ * token's position (MoE comm bottleneck, section 1.1, the combine step).
+ * y[t] = bf16(sum_{j: dest_row[t,j] >= 0, ascending j} topk_w[t,j] *
+ * y_perm[dest_row[t,j]]), fp32 accumulation; a token with no kept slot gets
+ * zeros. Needs no workspace. */
+moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t* dest_row,
+                       const float* topk_w, moe_bf16* y, void* stream);
+
+/* The whole layer forward: route, dispatch, expert FFN and combine on one
+ * stream, with no host synchronisation.
+ *   in : x, gate, gate_bias (or NULL), W1, W2 as above
+ *   out: y [T,H] bf16 (required); aux, topk_idx, topk_w, routed_counts, P,
+ *        kept_counts, offsets, dest_row may each be NULL (then kept in ws).
+ *   events: NULL, or MOE_LAYER_NUM_EVENTS cudaEvent_t handles (host
+ *        pointer to an array); events[0] is recorded before the first
+ *        kernel and events[1..6] after the route, scan, permute, FFN GEMM1,
+ *        FFN GEMM2 and combine stages, for per-stage timing. */
+moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                         const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                         moe_bf16* y, float* aux, int32_t* topk_idx, float* topk_w,
+                         int32_t* routed_counts, float* P, int32_t* kept_counts,
+                         int32_t* offsets, int32_t* dest_row, uint32_t* dev_status,
+                         void* ws, size_t ws_bytes, void* stream, void* const* events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,69 @@
+"""Shared test utilities: conversions, tolerance checks and the oracle
+applied in chunks for full-size workloads. Test infrastructure only."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+
+# spec floating-point bars for bf16-in / fp32-accumulate outputs
+FFN_MAX_REL = 2e-2      # max|err| <= 2e-2 * max|ref|
+FFN_MEAN_REL = 5e-3     # sum|err| <= 5e-3 * sum|ref|   (mean relative error)
+W_ABS = 1e-6            # routing weights
+STAT_REL = 1e-5         # P and aux
+NEAR_TIE = 1e-5         # top-k margin below which a routing flip is logged
+
+
+def np64(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 copy of a (bf16 / fp32) tensor."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_ffn_close(got: np.ndarray, ref: np.ndarray, what: str = "output"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    if ref.size == 0:
+        return
+    err = np.abs(got - ref)
+    scale = np.abs(ref).max()
+    assert err.max() <= FFN_MAX_REL * scale + 1e-30, \
+        f"{what}: max|err| {err.max():.3e} > {FFN_MAX_REL} * {scale:.3e}"
+    mean_rel = err.sum() / max(np.abs(ref).sum(), 1e-30)
+    assert mean_rel <= FFN_MEAN_REL, f"{what}: mean relative error {mean_rel:.3e}"
+
+
+def oracle_logits_chunked(x: torch.Tensor, gate: torch.Tensor, bias, rows=None,
+                          chunk: int = 8192) -> np.ndarray:
+    """Oracle router logits for all tokens (or the given rows), computed in
+    row chunks so float64 copies stay small. Row-wise, so chunking does not
+    change any value."""
+    g = np64(gate)
+    b = None if bias is None else bias.detach().cpu().numpy().astype(np.float32)
+    idx = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
+    out = np.empty((len(idx), g.shape[1]), np.float32)
+    for s in range(0, len(idx), chunk):
+        sel = torch.from_numpy(idx[s:s + chunk])
+        out[s:s + chunk] = O.router_logits(np64(x[sel]), g, b)
+    return out
+
+
+def topk_margins(logits: np.ndarray, k: int) -> np.ndarray:
+    """Smallest gap between consecutive entries of the sorted top-(k+1)
+    logits of each token: the decisions a rounding change can flip."""
+    lg = np.asarray(logits, np.float64)
+    s = -np.sort(-lg, axis=1)[:, :min(k + 1, lg.shape[1])]
+    if s.shape[1] < 2:
+        return np.full(lg.shape[0], np.inf)
+    return np.min(s[:, :-1] - s[:, 1:], axis=1)
+
+
+def bf16_tensor(a: np.ndarray) -> torch.Tensor:
+    """float64 values that are bf16-exact -> bf16 tensor (CPU)."""
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def fill_nan_bf16(t: torch.Tensor):
+    t.view(torch.int16).fill_(0x7FC0)

@@ -1,0 +1,122 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+the header declares, and its host-side logic (capacity, workspace size,
+argument checks that run before any launch) behaves. No compute calls."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import top_routing_expert_gb300 as moe
+import workloads as W
+from oracle import moe_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(moe_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_fwd"]:
+        assert n in names
+    assert set(names) == set(moe.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.moe_abi_version() == 1
+
+
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+def test_capacity_matches_oracle_on_workloads(lib, name):
+    w = W.get(name)
+    assert moe.capacity(w.T, w.E, w.k, w.cf) == O.capacity(w.T, w.E, w.k, w.cf)
+
+
+def test_capacity_edge_cases(lib):
+    rng_cases = [(0, 4, 2, 1.0), (1, 256, 1, 0.01), (7, 3, 2, 0.5), (1000, 12, 3, 1.0),
+                 (131072, 128, 2, 1.1), (10, 1, 1, 1.1), (3, 7, 3, 3.3)]
+    for T, E, k, cf in rng_cases:
+        assert moe.capacity(T, E, k, cf) == O.capacity(T, E, k, cf)
+    assert moe.capacity(5, 0, 1, 1.0) == -1
+    assert moe.capacity(5, 4, 1, float("nan")) == -1
+    assert moe.capacity(5, 4, 1, -1.0) == -1
+
+
+def _shape(T=64, H=128, E=8, k=2, h=128, cf=1.25):
+    return moe.MoeShape.make(T, H, E, k, h, cf)
+
+
+def _status(lib, s):
+    n = ctypes.c_size_t()
+    return lib.moe_workspace_size(ctypes.byref(s) if s is not None else None, ctypes.byref(n)), n.value
+
+
+def test_workspace_size_and_shape_checks(lib):
+    st, n = _status(lib, _shape())
+    assert st == 0 and n > 0
+    big = _status(lib, _shape(T=32768, H=4096, E=8, k=2, h=14336))[1]
+    # holds at least x_perm, act and y_perm for T*k rows
+    assert big >= 65536 * (4096 + 14336 + 4096) * 2
+    assert _status(lib, None)[0] == 1                       # NULL
+    assert _status(lib, _shape(T=-1))[0] == 2               # SHAPE
+    assert _status(lib, _shape(cf=0.0))[0] == 2
+    assert _status(lib, _shape(cf=float("inf")))[0] == 2
+    assert _status(lib, _shape(E=257))[0] == 3              # UNSUPPORTED
+    assert _status(lib, _shape(k=9, E=16))[0] == 3
+    assert _status(lib, _shape(k=5, E=4))[0] == 3
+    assert _status(lib, _shape(H=100))[0] == 3
+    assert _status(lib, _shape(h=96))[0] == 3
+    assert _status(lib, _shape(T=2 ** 30, k=2))[0] == 3
+    assert _status(lib, _shape(T=0))[0] == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails its host checks
+
+
+def test_entry_points_reject_bad_arguments_before_launch(lib):
+    s = _shape()
+    ws_need = _status(lib, s)[1]
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    # NULL required pointers
+    assert lib.moe_route(ctypes.byref(s), None, f, None, f, f, None, None, None, None, None,
+                         f, ws_need, None) == 1
+    assert lib.moe_layer_fwd(ctypes.byref(s), f, f, None, f, f, None, *[None] * 9,
+                             f, ws_need, None, None) == 1
+    assert lib.moe_combine(ctypes.byref(s), f, f, f, None, None) == 1
+    # misaligned pointers
+    assert lib.moe_combine(ctypes.byref(s), P(FAKE + 8), f, f, f, None) == 5
+    assert lib.moe_permute(ctypes.byref(s), f, f, None, f, f, None, P(FAKE + 2), None, f,
+                           ws_need, None) == 5
+    # workspace too small / missing
+    assert lib.moe_route_logits(ctypes.byref(s), f, f, f, None, None, None, None, f,
+                                ws_need - 1, None) == 4
+    assert lib.moe_permute(ctypes.byref(s), f, f, None, f, f, None, f, None, None, 0, None) == 1
+    # bad shapes
+    bad = _shape(E=300)
+    assert lib.moe_expert_ffn(ctypes.byref(bad), f, f, f, f, f, f, f, None, 0, None) == 3
+    assert lib.moe_combine(None, f, f, f, f, None) == 1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert moe.status_str(code)
+    assert moe.status_str(0) == "ok"

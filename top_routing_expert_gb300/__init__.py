@@ -1,0 +1,236 @@
+"""Python binding of the GB300 MoE layer-forward library (C ABI in
+include/moe_gb300.h). Argument marshalling only: every step of the layer
+runs in the library's CUDA kernels, on the current torch CUDA stream.
+
+The functions carry the C names. Tensors must be contiguous CUDA tensors of
+the dtypes below; outputs are written in place. A non-OK status raises
+``MoeError``. There is no CPU path: without the built library (see
+``build()``) importing the native layer fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from ._build import LIB, build  # noqa: F401  (re-exported)
+
+__all__ = [
+    "MoeError", "MoeShape", "load_library", "capacity", "workspace_size", "status_str",
+    "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
+    "moe_combine", "moe_layer_fwd", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
+    "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
+]
+
+DEV_BAD_INDEX, DEV_DUP_INDEX, DEV_NONFINITE, DEV_TIMEOUT = 1, 2, 4, 8
+LAYER_NUM_EVENTS = 7
+EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "moe_status_str",
+                    "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
+                    "moe_combine", "moe_layer_fwd"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn} failed: status {code} ({text})")
+        self.code = code
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("E", ctypes.c_int64),
+                ("top_k", ctypes.c_int64), ("h", ctypes.c_int64),
+                ("capacity_factor", ctypes.c_double)]
+
+    @classmethod
+    def make(cls, T, H, E, k, h, cf) -> "MoeShape":
+        return cls(int(T), int(H), int(E), int(k), int(h), float(cf))
+
+
+_lib: Optional[ctypes.CDLL] = None
+_P = ctypes.c_void_p
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads the built library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or os.environ.get("MOE_GB300_LIB", LIB)
+    if not os.path.exists(path):
+        raise RuntimeError(f"native library {path} is missing: run top_routing_expert_gb300.build()")
+    lib = ctypes.CDLL(path)
+    S = ctypes.POINTER(MoeShape)
+    lib.moe_abi_version.restype = ctypes.c_int
+    lib.moe_capacity.restype = ctypes.c_int64
+    lib.moe_capacity.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double]
+    lib.moe_workspace_size.restype = ctypes.c_int
+    lib.moe_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_status_str.restype = ctypes.c_char_p
+    lib.moe_status_str.argtypes = [ctypes.c_int]
+    lib.moe_route.restype = ctypes.c_int
+    lib.moe_route.argtypes = [S] + [_P] * 11 + [ctypes.c_size_t, _P]
+    lib.moe_route_logits.restype = ctypes.c_int
+    lib.moe_route_logits.argtypes = [S] + [_P] * 8 + [ctypes.c_size_t, _P]
+    lib.moe_permute.restype = ctypes.c_int
+    lib.moe_permute.argtypes = [S] + [_P] * 9 + [ctypes.c_size_t, _P]
+    lib.moe_expert_ffn.restype = ctypes.c_int
+    lib.moe_expert_ffn.argtypes = [S] + [_P] * 8 + [ctypes.c_size_t, _P]
+    lib.moe_combine.restype = ctypes.c_int
+    lib.moe_combine.argtypes = [S] + [_P] * 5
+    lib.moe_layer_fwd.restype = ctypes.c_int
+    lib.moe_layer_fwd.argtypes = [S] + [_P] * 16 + [ctypes.c_size_t, _P, _P]
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ helpers ----
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MoeError(fn, code, status_str(code))
+
+
+def _shape(s) -> MoeShape:
+    if isinstance(s, MoeShape):
+        return s
+    if isinstance(s, dict):
+        return MoeShape.make(s["T"], s["H"], s["E"], s["k"], s["h"], s["cf"])
+    return MoeShape.make(*s)
+
+
+# ---------------------------------------------------------- host calls ----
+
+def abi_version() -> int:
+    return load_library().moe_abi_version()
+
+
+def capacity(T: int, E: int, k: int, cf: float) -> int:
+    return load_library().moe_capacity(T, E, k, cf)
+
+
+def status_str(code: int) -> str:
+    return load_library().moe_status_str(code).decode()
+
+
+def workspace_size(shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size", load_library().moe_workspace_size(ctypes.byref(_shape(shape)), ctypes.byref(n)))
+    return n.value
+
+
+class Workspace:
+    """Caller-owned device scratch for one shape (a torch uint8 tensor)."""
+
+    def __init__(self, shape, device="cuda"):
+        self.shape = _shape(shape)
+        self.nbytes = workspace_size(self.shape)
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+
+def _ws(ws: Workspace | None, shape: MoeShape):
+    if ws is None:
+        return None, 0
+    return ws.ptr, ws.nbytes
+
+
+# ------------------------------------------------------------ kernels ----
+
+def moe_route(shape, x, gate, gate_bias, topk_idx, topk_w, routed_counts=None, P=None,
+              aux=None, logits_out=None, dev_status=None, ws: Workspace | None = None,
+              stream=None):
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_route", load_library().moe_route(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
+        _ptr(P, torch.float32, "P"), _ptr(aux, torch.float32, "aux"),
+        _ptr(logits_out, torch.float32, "logits_out"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
+
+
+def moe_route_logits(shape, logits, topk_idx, topk_w, routed_counts=None, P=None, aux=None,
+                     dev_status=None, ws: Workspace | None = None, stream=None):
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_route_logits", load_library().moe_route_logits(
+        ctypes.byref(s), _ptr(logits, torch.float32, "logits"),
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
+        _ptr(aux, torch.float32, "aux"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
+
+
+def moe_permute(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x_perm,
+                dev_status=None, ws: Workspace | None = None, stream=None):
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_permute", load_library().moe_permute(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
+        _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
+
+
+def moe_expert_ffn(shape, x_perm, offsets, W1, W2, act, y_perm, dev_status=None,
+                   ws: Workspace | None = None, stream=None):
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_expert_ffn", load_library().moe_expert_ffn(
+        ctypes.byref(s), _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(W1, torch.bfloat16, "W1"), _ptr(W2, torch.bfloat16, "W2"),
+        _ptr(act, torch.bfloat16, "act"), _ptr(y_perm, torch.bfloat16, "y_perm"),
+        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+
+
+def moe_combine(shape, y_perm, dest_row, topk_w, y, stream=None):
+    s = _shape(shape)
+    _check("moe_combine", load_library().moe_combine(
+        ctypes.byref(s), _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dest_row, torch.int32, "dest_row"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(y, torch.bfloat16, "y"), _stream(stream)))
+
+
+def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None, topk_w=None,
+                  routed_counts=None, P=None, kept_counts=None, offsets=None, dest_row=None,
+                  dev_status=None, ws: Workspace | None = None, stream=None,
+                  events: Optional[Sequence[torch.cuda.Event]] = None):
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    ev = None
+    if events is not None:
+        if len(events) != LAYER_NUM_EVENTS:
+            raise ValueError(f"events must hold {LAYER_NUM_EVENTS} torch.cuda.Event")
+        ev = (ctypes.c_void_p * LAYER_NUM_EVENTS)(*[e.cuda_event for e in events])
+    _check("moe_layer_fwd", load_library().moe_layer_fwd(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
+        _ptr(W2, torch.bfloat16, "W2"), _ptr(y, torch.bfloat16, "y"), _ptr(aux, torch.float32, "aux"),
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
+        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream), ev))

@@ -1,0 +1,560 @@
+// Host side of the C ABI declared in include/moe_gb300.h: argument checks,
+// workspace carve-up, TMA descriptor encoding and the launch sequence of
+// each entry point. Nothing here allocates device memory or synchronises
+// with the device.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+// ---------------------------------------------------------------- checks ----
+
+constexpr int64_t kMaxDim = 65536;
+
+moe_status check_shape(const moe_shape* s) {
+  if (s == nullptr) return MOE_ERR_NULL;
+  if (s->T < 0 || s->H <= 0 || s->E <= 0 || s->top_k <= 0 || s->h <= 0) return MOE_ERR_SHAPE;
+  if (!isfinite(s->capacity_factor) || !(s->capacity_factor > 0.0)) return MOE_ERR_SHAPE;
+  if (s->E > kMaxExperts || s->top_k > kMaxTopK || s->top_k > s->E) return MOE_ERR_UNSUPPORTED;
+  if (s->H % 64 != 0 || s->h % 64 != 0 || s->H > kMaxDim || s->h > kMaxDim)
+    return MOE_ERR_UNSUPPORTED;
+  if (s->T > (int64_t(1) << 31) || s->T * s->top_k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define MOE_REQUIRE(p) \
+  do {                 \
+    if ((p) == nullptr) return MOE_ERR_NULL; \
+    if (!aligned16(p)) return MOE_ERR_ALIGN; \
+  } while (0)
+
+#define MOE_OPTIONAL(p) \
+  do {                  \
+    if ((p) != nullptr && !aligned16(p)) return MOE_ERR_ALIGN; \
+  } while (0)
+
+#define MOE_CUDA(x)                                \
+  do {                                             \
+    if ((x) != cudaSuccess) return MOE_ERR_CUDA;   \
+  } while (0)
+
+// ------------------------------------------------------------- workspace ----
+
+struct Ws {
+  uint16_t* gateT;
+  int32_t* tile_cnt;
+  int32_t* tile_base;
+  uint8_t* rank8;
+  float* ppart;
+  int32_t* routed;
+  float* P;
+  float* aux;
+  int32_t* kept;
+  int32_t* offsets;
+  uint32_t* status;
+  uint32_t* ticket;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* dest_row;
+  int32_t* src_token;
+  uint16_t* x_perm;
+  uint16_t* act;
+  uint16_t* y_perm;
+};
+
+struct Dims {
+  int T, H, E, k, h, E_pad, n_tiles;
+  int64_t A, C;
+};
+
+Dims dims_of(const moe_shape* s) {
+  Dims d;
+  d.T = static_cast<int>(s->T);
+  d.H = static_cast<int>(s->H);
+  d.E = static_cast<int>(s->E);
+  d.k = static_cast<int>(s->top_k);
+  d.h = static_cast<int>(s->h);
+  d.E_pad = (d.E + 15) & ~15;
+  d.n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
+  d.A = s->T * s->top_k;
+  d.C = moe_capacity(s->T, s->E, s->top_k, s->capacity_factor);
+  return d;
+}
+
+// Lays the scratch arrays out from `base` (256-byte aligned pieces); with
+// base == nullptr only the size is computed.
+size_t layout(const Dims& d, uint8_t* base, Ws* w) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? base + off : nullptr;
+    off += (bytes + 255) & ~size_t(255);
+    return p;
+  };
+  const size_t A = static_cast<size_t>(d.A);
+  const size_t ET = static_cast<size_t>(d.E) * d.n_tiles;
+  Ws v;
+  v.gateT = static_cast<uint16_t*>(take(static_cast<size_t>(d.E_pad) * d.H * 2));
+  v.tile_cnt = static_cast<int32_t*>(take(ET * 4));
+  v.tile_base = static_cast<int32_t*>(take(ET * 4));
+  v.rank8 = static_cast<uint8_t*>(take(A));
+  v.ppart = static_cast<float*>(take(ET * 4));
+  v.routed = static_cast<int32_t*>(take(static_cast<size_t>(d.E) * 4));
+  v.P = static_cast<float*>(take(static_cast<size_t>(d.E) * 4));
+  v.aux = static_cast<float*>(take(4));
+  v.kept = static_cast<int32_t*>(take(static_cast<size_t>(d.E) * 4));
+  v.offsets = static_cast<int32_t*>(take(static_cast<size_t>(d.E + 1) * 4));
+  v.status = static_cast<uint32_t*>(take(4));
+  v.ticket = static_cast<uint32_t*>(take(4));
+  v.topk_idx = static_cast<int32_t*>(take(A * 4));
+  v.topk_w = static_cast<float*>(take(A * 4));
+  v.dest_row = static_cast<int32_t*>(take(A * 4));
+  v.src_token = static_cast<int32_t*>(take(A * 4));
+  v.x_perm = static_cast<uint16_t*>(take(A * d.H * 2));
+  v.act = static_cast<uint16_t*>(take(A * d.h * 2));
+  v.y_perm = static_cast<uint16_t*>(take(A * d.H * 2));
+  if (w) *w = v;
+  return off;
+}
+
+moe_status carve(const moe_shape* s, const Dims& d, void* ws, size_t ws_bytes, Ws* w) {
+  const size_t need = layout(d, nullptr, nullptr);
+  if (ws == nullptr) return MOE_ERR_NULL;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  layout(d, static_cast<uint8_t*>(ws), w);
+  (void)s;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------ device queries ----
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* e = getenv("MOE_GB300_WAIT_TIMEOUT_NS");
+    if (e != nullptr) {
+      const unsigned long long x = strtoull(e, nullptr, 10);
+      if (x > 0) return static_cast<uint64_t>(x);
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------ TMA maps ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A bf16 row-major matrix [outer, inner] read in boxes of box_outer rows x
+// box_inner (= 64, one 128-byte swizzle row) columns.
+bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t gdim[2] = {inner, outer};
+  const cuuint64_t gstride[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- stages ----
+
+struct RouteOut {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* routed;
+  float* P;
+  float* aux;
+  float* logits_out;
+};
+
+moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, const float* bias,
+                     const float* logits_in, const RouteOut& o, uint32_t* status, const Ws& w,
+                     cudaStream_t st) {
+  if (d.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(o.routed, 0, sizeof(int32_t) * d.E, st));
+    MOE_CUDA(cudaMemsetAsync(o.P, 0, sizeof(float) * d.E, st));
+    if (o.aux) MOE_CUDA(cudaMemsetAsync(o.aux, 0, sizeof(float), st));
+    return MOE_OK;
+  }
+  RouteArgs a;
+  a.T = d.T;
+  a.H = d.H;
+  a.E = d.E;
+  a.E_pad = d.E_pad;
+  a.k = d.k;
+  a.n_tiles = d.n_tiles;
+  a.stages = route_stages(d.E_pad);
+  a.bias = bias;
+  a.logits_in = logits_in;
+  a.topk_idx = o.topk_idx;
+  a.topk_w = o.topk_w;
+  a.logits_out = o.logits_out;
+  a.tile_cnt = w.tile_cnt;
+  a.rank8 = w.rank8;
+  a.ppart = w.ppart;
+  a.ticket = w.ticket;
+  a.dev_status = status;
+  a.timeout_ns = wait_timeout_ns();
+  if (logits_in != nullptr) {
+    MOE_CUDA(launch_route_logits(a, st));
+  } else {
+    MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
+    CUtensorMap tm_x, tm_g;
+    if (!tmap_bf16_2d(&tm_x, x, d.H, d.T, kBlockK, kTileTokens)) return MOE_ERR_CUDA;
+    if (!tmap_bf16_2d(&tm_g, w.gateT, d.H, d.E_pad, kBlockK, d.E_pad)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_route_gemm(tm_x, tm_g, a, st));
+  }
+  return MOE_OK;
+}
+
+moe_status run_scan(const Dims& d, bool with_stats, int32_t* routed, float* P, float* aux,
+                    int32_t* kept, int32_t* offsets, const Ws& w, cudaStream_t st) {
+  ScanArgs s;
+  s.T = d.T;
+  s.E = d.E;
+  s.k = d.k;
+  s.n_tiles = d.n_tiles;
+  s.C = d.C;
+  s.tile_cnt = w.tile_cnt;
+  s.tile_base = w.tile_base;
+  s.ppart = with_stats ? w.ppart : nullptr;
+  s.routed = routed;
+  s.P = P;
+  s.aux = with_stats ? aux : nullptr;
+  s.kept = kept;
+  s.offsets = offsets;
+  s.ticket = w.ticket;
+  MOE_CUDA(launch_scan(s, st));
+  return MOE_OK;
+}
+
+moe_status run_gather(const Dims& d, const moe_bf16* x, const int32_t* idx, const int32_t* offsets,
+                      int32_t* dest_row, int32_t* src_token, moe_bf16* x_perm, uint32_t* status,
+                      const Ws& w, cudaStream_t st) {
+  GatherArgs g;
+  g.T = d.T;
+  g.H = d.H;
+  g.E = d.E;
+  g.k = d.k;
+  g.n_tiles = d.n_tiles;
+  g.C = d.C;
+  g.x = x;
+  g.topk_idx = idx;
+  g.rank8 = w.rank8;
+  g.tile_base = w.tile_base;
+  g.offsets = offsets;
+  g.dest_row = dest_row;
+  g.src_token = src_token;
+  g.x_perm = x_perm;
+  g.dev_status = status;
+  MOE_CUDA(launch_gather(g, num_sms(), st));
+  return MOE_OK;
+}
+
+moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const int32_t* offsets,
+                    int K, int N, moe_bf16* D, int gelu, uint32_t* status, cudaStream_t st) {
+  if (d.A == 0) return MOE_OK;
+  CUtensorMap tm_a, tm_b;
+  if (!tmap_bf16_2d(&tm_a, A, K, d.A, kBlockK, 128)) return MOE_ERR_CUDA;
+  if (!tmap_bf16_2d(&tm_b, W, N, static_cast<uint64_t>(d.E) * K, 64, kBlockK)) return MOE_ERR_CUDA;
+  GemmArgs g;
+  g.offsets = offsets;
+  g.E = d.E;
+  g.K = K;
+  g.N = N;
+  g.rows = static_cast<int>(d.A);
+  g.D = D;
+  g.gelu = gelu;
+  g.dev_status = status;
+  g.timeout_ns = wait_timeout_ns();
+  MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));
+  return MOE_OK;
+}
+
+moe_status run_combine(const Dims& d, const moe_bf16* y_perm, const int32_t* dest_row,
+                       const float* topk_w, moe_bf16* y, cudaStream_t st) {
+  CombineArgs c;
+  c.T = d.T;
+  c.H = d.H;
+  c.k = d.k;
+  c.y_perm = y_perm;
+  c.dest_row = dest_row;
+  c.topk_w = topk_w;
+  c.y = y;
+  MOE_CUDA(launch_combine(c, num_sms(), st));
+  return MOE_OK;
+}
+
+#define MOE_TRY(x)                         \
+  do {                                     \
+    const moe_status _s = (x);             \
+    if (_s != MOE_OK) return _s;           \
+  } while (0)
+
+}  // namespace
+
+// ================================================================ ABI ====
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_GB300_ABI_VERSION; }
+
+int64_t moe_capacity(int64_t T, int64_t E, int64_t top_k, double capacity_factor) {
+  if (T < 0 || E < 1 || top_k < 1 || !isfinite(capacity_factor) || !(capacity_factor > 0.0))
+    return -1;
+  const double c = ceil(capacity_factor * static_cast<double>(T * top_k) / static_cast<double>(E));
+  const int64_t ci = static_cast<int64_t>(c);
+  return ci < 1 ? 1 : ci;
+}
+
+const char* moe_status_str(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "invalid shape or capacity factor";
+    case MOE_ERR_UNSUPPORTED: return "shape outside the supported ranges";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_size";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA call or kernel launch failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_workspace_size(const moe_shape* s, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_NULL;
+  MOE_TRY(check_shape(s));
+  *bytes = layout(dims_of(s), nullptr, nullptr);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                     const float* gate_bias, int32_t* topk_idx, float* topk_w,
+                     int32_t* routed_counts, float* P, float* aux, float* logits_out,
+                     uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(gate);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(topk_w);
+  MOE_OPTIONAL(gate_bias);
+  MOE_OPTIONAL(routed_counts);
+  MOE_OPTIONAL(P);
+  MOE_OPTIONAL(aux);
+  MOE_OPTIONAL(logits_out);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteOut o{topk_idx, topk_w, routed_counts ? routed_counts : w.routed, P ? P : w.P, aux,
+             logits_out};
+  uint32_t* status = dev_status ? dev_status : w.status;
+  MOE_TRY(run_route(d, x, gate, gate_bias, nullptr, o, status, w, st));
+  if (d.T > 0) MOE_TRY(run_scan(d, true, o.routed, o.P, aux, nullptr, nullptr, w, st));
+  return MOE_OK;
+}
+
+moe_status moe_route_logits(const moe_shape* s, const float* logits, int32_t* topk_idx,
+                            float* topk_w, int32_t* routed_counts, float* P, float* aux,
+                            uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(logits);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(topk_w);
+  MOE_OPTIONAL(routed_counts);
+  MOE_OPTIONAL(P);
+  MOE_OPTIONAL(aux);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteOut o{topk_idx, topk_w, routed_counts ? routed_counts : w.routed, P ? P : w.P, aux,
+             nullptr};
+  uint32_t* status = dev_status ? dev_status : w.status;
+  MOE_TRY(run_route(d, nullptr, nullptr, nullptr, logits, o, status, w, st));
+  if (d.T > 0) MOE_TRY(run_scan(d, true, o.routed, o.P, aux, nullptr, nullptr, w, st));
+  return MOE_OK;
+}
+
+moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+                       int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                       int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status, void* ws,
+                       size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(dest_row);
+  MOE_REQUIRE(x_perm);
+  MOE_OPTIONAL(kept_counts);
+  MOE_OPTIONAL(src_token);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = dev_status ? dev_status : w.status;
+  if (d.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), st));
+    if (kept_counts) MOE_CUDA(cudaMemsetAsync(kept_counts, 0, sizeof(int32_t) * d.E, st));
+    return MOE_OK;
+  }
+  RankArgs r;
+  r.T = d.T;
+  r.E = d.E;
+  r.k = d.k;
+  r.n_tiles = d.n_tiles;
+  r.topk_idx = topk_idx;
+  r.tile_cnt = w.tile_cnt;
+  r.rank8 = w.rank8;
+  r.ticket = w.ticket;
+  r.dev_status = status;
+  MOE_CUDA(launch_rank(r, st));
+  MOE_TRY(run_scan(d, false, w.routed, w.P, nullptr, kept_counts, offsets, w, st));
+  MOE_TRY(run_gather(d, x, topk_idx, offsets, dest_row, src_token, x_perm, status, w, st));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int32_t* offsets,
+                          const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
+                          moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                          void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x_perm);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(W1);
+  MOE_REQUIRE(W2);
+  MOE_REQUIRE(act);
+  MOE_REQUIRE(y_perm);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  uint32_t* status = dev_status;
+  if (status == nullptr) {
+    Ws w;
+    MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+    status = w.status;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(run_gemm(d, x_perm, W1, offsets, d.H, d.h, act, 1, status, st));
+  MOE_TRY(run_gemm(d, act, W2, offsets, d.h, d.H, y_perm, 0, status, st));
+  return MOE_OK;
+}
+
+moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t* dest_row,
+                       const float* topk_w, moe_bf16* y, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(y_perm);
+  MOE_REQUIRE(dest_row);
+  MOE_REQUIRE(topk_w);
+  MOE_REQUIRE(y);
+  const Dims d = dims_of(s);
+  return run_combine(d, y_perm, dest_row, topk_w, y, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                         const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                         moe_bf16* y, float* aux, int32_t* topk_idx, float* topk_w,
+                         int32_t* routed_counts, float* P, int32_t* kept_counts,
+                         int32_t* offsets, int32_t* dest_row, uint32_t* dev_status, void* ws,
+                         size_t ws_bytes, void* stream, void* const* events) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(gate);
+  MOE_REQUIRE(W1);
+  MOE_REQUIRE(W2);
+  MOE_REQUIRE(y);
+  MOE_OPTIONAL(gate_bias);
+  MOE_OPTIONAL(aux);
+  MOE_OPTIONAL(topk_idx);
+  MOE_OPTIONAL(topk_w);
+  MOE_OPTIONAL(routed_counts);
+  MOE_OPTIONAL(P);
+  MOE_OPTIONAL(kept_counts);
+  MOE_OPTIONAL(offsets);
+  MOE_OPTIONAL(dest_row);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = dev_status ? dev_status : w.status;
+  int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
+  float* wts = topk_w ? topk_w : w.topk_w;
+  int32_t* routed = routed_counts ? routed_counts : w.routed;
+  float* Pp = P ? P : w.P;
+  int32_t* kept = kept_counts ? kept_counts : w.kept;
+  int32_t* off = offsets ? offsets : w.offsets;
+  int32_t* dest = dest_row ? dest_row : w.dest_row;
+  auto mark = [&](int i) -> bool {
+    return events == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (d.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(routed, 0, sizeof(int32_t) * d.E, st));
+    MOE_CUDA(cudaMemsetAsync(Pp, 0, sizeof(float) * d.E, st));
+    MOE_CUDA(cudaMemsetAsync(kept, 0, sizeof(int32_t) * d.E, st));
+    MOE_CUDA(cudaMemsetAsync(off, 0, sizeof(int32_t) * (d.E + 1), st));
+    if (aux) MOE_CUDA(cudaMemsetAsync(aux, 0, sizeof(float), st));
+    for (int i = 1; i < MOE_LAYER_NUM_EVENTS; ++i)
+      if (!mark(i)) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  RouteOut o{idx, wts, routed, Pp, aux, nullptr};
+  MOE_TRY(run_route(d, x, gate, gate_bias, nullptr, o, status, w, st));
+  if (!mark(1)) return MOE_ERR_CUDA;
+  MOE_TRY(run_scan(d, true, routed, Pp, aux, kept, off, w, st));
+  if (!mark(2)) return MOE_ERR_CUDA;
+  MOE_TRY(run_gather(d, x, idx, off, dest, w.src_token, w.x_perm, status, w, st));
+  if (!mark(3)) return MOE_ERR_CUDA;
+  MOE_TRY(run_gemm(d, w.x_perm, W1, off, d.H, d.h, w.act, 1, status, st));
+  if (!mark(4)) return MOE_ERR_CUDA;
+  MOE_TRY(run_gemm(d, w.act, W2, off, d.h, d.H, w.y_perm, 0, status, st));
+  if (!mark(5)) return MOE_ERR_CUDA;
+  MOE_TRY(run_combine(d, w.y_perm, dest, wts, y, st));
+  if (!mark(6)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// Internal interface between the host entry points (moe_api.cu) and the
+// kernel files. Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+constexpr int kTileTokens = 128;  // tokens per routing tile = router GEMM M
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 256;
+constexpr int kBlockK = 64;       // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+// Router epilogue arguments (GEMM and logits entry points).
+struct RouteArgs {
+  int T, H, E, E_pad, k, n_tiles, stages;
+  const float* bias;       // [E] or nullptr (GEMM path only)
+  const float* logits_in;  // [T,E] (logits path only)
+  int32_t* topk_idx;       // [T,k]
+  float* topk_w;           // [T,k]
+  float* logits_out;       // [T,E] or nullptr
+  int32_t* tile_cnt;       // [E][n_tiles] assignments per routing tile
+  uint8_t* rank8;          // [T*k] rank of the token among its tile's tokens of that expert
+  float* ppart;            // [E][n_tiles] sum of p over the tile's tokens
+  uint32_t* ticket;        // reset to 0 by block 0 (used by the scan)
+  uint32_t* dev_status;
+  uint64_t timeout_ns;
+};
+
+// Tile counts and ranks from caller-given indices (dispatch without route).
+struct RankArgs {
+  int T, E, k, n_tiles;
+  const int32_t* topk_idx;
+  int32_t* tile_cnt;
+  uint8_t* rank8;
+  uint32_t* ticket;
+  uint32_t* dev_status;
+};
+
+struct ScanArgs {
+  int T, E, k, n_tiles;
+  int64_t C;
+  const int32_t* tile_cnt;  // [E][n_tiles]
+  int32_t* tile_base;       // [E][n_tiles] exclusive prefix over tiles
+  const float* ppart;       // [E][n_tiles] or nullptr (no P / aux)
+  int32_t* routed;          // [E]
+  float* P;                 // [E]
+  float* aux;               // [1] or nullptr
+  int32_t* kept;            // [E] or nullptr
+  int32_t* offsets;         // [E+1] or nullptr
+  uint32_t* ticket;
+};
+
+struct GatherArgs {
+  int T, H, E, k, n_tiles;
+  int64_t C;
+  const uint16_t* x;
+  const int32_t* topk_idx;
+  const uint8_t* rank8;
+  const int32_t* tile_base;
+  const int32_t* offsets;
+  int32_t* dest_row;
+  int32_t* src_token;  // or nullptr
+  uint16_t* x_perm;
+  uint32_t* dev_status;
+};
+
+struct CombineArgs {
+  int T, H, k;
+  const uint16_t* y_perm;
+  const int32_t* dest_row;
+  const float* topk_w;
+  uint16_t* y;
+};
+
+// TMEM columns the router allocates: a power of two >= 32 covering E_pad.
+__host__ __device__ inline int route_tmem_cols(int E_pad) {
+  int c = 32;
+  while (c < E_pad) c <<= 1;
+  return c;
+}
+
+struct GemmArgs {
+  const int32_t* offsets;  // [E+1] row segments of the expert-major buffer
+  int E, K, N;             // reduction size, output columns
+  int rows;                // rows of the A and D buffers (T*k)
+  uint16_t* D;             // [rows, N] bf16
+  int gelu;                // 1: act = gelu_tanh(acc), 0: plain
+  uint32_t* dev_status;
+  uint64_t timeout_ns;
+};
+
+int route_stages(int E_pad);
+size_t route_smem_bytes(int E_pad, int stages);
+size_t gemm_smem_bytes(int E);
+
+cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, int E, int E_pad,
+                                  cudaStream_t st);
+cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                              const RouteArgs& a, cudaStream_t st);
+cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st);
+cudaError_t launch_rank(const RankArgs& a, cudaStream_t st);
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);
+cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const GemmArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace moe

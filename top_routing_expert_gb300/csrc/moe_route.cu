@@ -1,0 +1,448 @@
+// Router: logits GEMM on the tensor cores (tcgen05, accumulator in TMEM)
+// fused with the routing epilogue - softmax over E, top-k with renormalised
+// weights, per-tile partial sums of the probabilities, per-tile expert
+// histograms and in-tile arrival ranks (MoE module notes, section 3.1 router
+// listing; MoE comm bottleneck, section 3.2 auxiliary-loss statistics).
+//
+// One CTA = one tile of 128 tokens = one UMMA M. Thread r of the CTA owns
+// token row r, which is TMEM lane r, so softmax and top-k need no
+// cross-thread exchange.
+#include <math.h>
+
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+// ----------------------------------------------------------- top-k list ----
+
+// A descending list of the k best (logit, expert) pairs in registers. A new
+// pair displaces an entry only if its logit is strictly larger, so among
+// equal logits the lower expert index (seen first) stays ahead.
+struct TopK {
+  float v[kMaxTopK];
+  int i[kMaxTopK];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      v[j] = -INFINITY;
+      i[j] = -1;
+    }
+  }
+  __device__ __forceinline__ void insert(float cv, int ce, int k) {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const bool gt = cv > v[j];
+        const float ov = v[j];
+        const int oi = i[j];
+        v[j] = gt ? cv : ov;
+        i[j] = gt ? ce : oi;
+        cv = gt ? ov : cv;
+        ce = gt ? oi : ce;
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------- tile ranks / counts --
+
+// Called by all 128 threads of a routing tile. `e[j]` (j < k) is the
+// thread's expert for slot j or -1 for an unusable slot. Produces for every
+// slot the number of earlier tokens of the tile that chose the same expert
+// (warp bit masks in shared memory, OR-ed, so the result does not depend on
+// thread timing) and writes the tile's per-expert counts.
+__device__ __forceinline__ void tile_ranks(uint32_t* masks, int E_stride, int E, int k,
+                                           const int (&e)[kMaxTopK], bool row_valid,
+                                           int (&rank)[kMaxTopK], int32_t* tile_cnt,
+                                           int n_tiles, int tile) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (row_valid) {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k && e[j] >= 0) atomicOr(&masks[warp * E_stride + e[j]], 1u << lane);
+  }
+  __syncthreads();
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    rank[j] = 0;
+    if (j < k && row_valid && e[j] >= 0) {
+      int r = __popc(masks[warp * E_stride + e[j]] & below);
+      for (int w = 0; w < warp; ++w) r += __popc(masks[w * E_stride + e[j]]);
+      rank[j] = r;
+    }
+  }
+  for (int x = tid; x < E; x += kTileTokens) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kTileTokens / 32; ++w) c += __popc(masks[w * E_stride + x]);
+    tile_cnt[static_cast<size_t>(x) * n_tiles + tile] = c;
+  }
+}
+
+// --------------------------------------------------------------- sources ----
+
+// Logits of the thread's row from TMEM (GEMM path), plus the gate bias.
+struct TmemSource {
+  uint32_t taddr;       // TMEM address of (this warp's lane quadrant, column 0)
+  const float* bias_s;  // shared, >= 32 * chunks entries, zero past E
+  __device__ __forceinline__ void load(int c, float (&v)[32]) const {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + 32u * c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + bias_s[32 * c + i];
+  }
+};
+
+// Logits of the thread's row from global memory (logits entry point).
+struct GlobalSource {
+  const float* row;
+  int E;
+  bool valid;
+  __device__ __forceinline__ void load(int c, float (&v)[32]) const {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 32 * c + i;
+      v[i] = (valid && e < E) ? row[e] : 0.f;
+    }
+  }
+};
+
+// The routing epilogue shared by both paths; identical arithmetic, so equal
+// logits give bit-identical results. All 128 threads call it.
+template <class Src>
+__device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
+                                               uint32_t* masks, float* red, int E_stride) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, k = a.k;
+  const int t = tile * kTileTokens + tid;
+  const bool valid = t < a.T;
+  const int nchunks = (E + 31) / 32;
+
+  // pass 1: top-k on the logits (its first entry is the max), finiteness
+  TopK tk;
+  tk.init();
+  bool bad = false;
+  float* lrow = (a.logits_out && valid) ? a.logits_out + static_cast<size_t>(t) * E : nullptr;
+  for (int c = 0; c < nchunks; ++c) {
+    float v[32];
+    src.load(c, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 32 * c + i;
+      if (e < E) {
+        bad |= !isfinite(v[i]);
+        tk.insert(v[i], e, k);
+        if (lrow) lrow[e] = v[i];
+      }
+    }
+  }
+  const float m = tk.v[0];
+
+  // pass 2: softmax denominator over all E experts, ascending e
+  float s = 0.f;
+  for (int c = 0; c < nchunks; ++c) {
+    float v[32];
+    src.load(c, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (32 * c + i < E) s += expf(v[i] - m);
+  }
+  const float inv_s = 1.0f / s;
+
+  // pass 3: per-expert sums of p over the tile's valid tokens (fixed
+  // butterfly within the warp, fixed warp order below)
+  for (int c = 0; c < nchunks; ++c) {
+    float v[32];
+    src.load(c, v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 32 * c + i;
+      if (e < E) {
+        float pe = valid ? expf(v[i] - m) * inv_s : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+        if (lane == 0) red[warp * E_stride + e] = pe;
+      }
+    }
+  }
+
+  // renormalised top-k weights: p_j / sum_j' p_j' = ex_j / sum ex_j'
+  float ex[kMaxTopK];
+  float den = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    ex[j] = (j < k && tk.i[j] >= 0) ? expf(tk.v[j] - m) : 0.f;
+    den += ex[j];
+  }
+
+  int rank[kMaxTopK];
+  tile_ranks(masks, E_stride, E, k, tk.i, valid, rank, a.tile_cnt, a.n_tiles, tile);
+
+  if (valid) {
+    const size_t base = static_cast<size_t>(t) * k;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        a.topk_idx[base + j] = tk.i[j];
+        a.topk_w[base + j] = ex[j] / den;
+        a.rank8[base + j] = static_cast<uint8_t>(rank[j]);
+      }
+    }
+    if (bad) atomicOr(a.dev_status, MOE_DEV_NONFINITE);
+  }
+  __syncthreads();
+  for (int x = tid; x < E; x += kTileTokens) {
+    float sum = red[x];
+#pragma unroll
+    for (int w = 1; w < kTileTokens / 32; ++w) sum += red[w * E_stride + x];
+    a.ppart[static_cast<size_t>(x) * a.n_tiles + tile] = sum;
+  }
+}
+
+// ---------------------------------------------------------------- kernels ---
+
+__global__ void gate_transpose_kernel(const uint16_t* __restrict__ gate,
+                                      uint16_t* __restrict__ gateT, int H, int E, int E_pad) {
+  const int64_t n = static_cast<int64_t>(E_pad) * H;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int e = static_cast<int>(i / H);
+    const int hh = static_cast<int>(i - static_cast<int64_t>(e) * H);
+    gateT[i] = e < E ? gate[static_cast<int64_t>(hh) * E + e] : uint16_t(0);
+  }
+}
+
+// Shared-memory carve-up of the router kernel (after the 1024-aligned
+// pipeline stages).
+struct RouteSmem {
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* done;
+  uint32_t* tmem_slot;
+  uint32_t* abort_flag;
+  float* bias_s;
+  uint32_t* masks;
+  float* red;
+};
+
+__device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, int E32) {
+  RouteSmem s;
+  s.full = reinterpret_cast<uint64_t*>(p);
+  s.empty = s.full + stages;
+  s.done = s.empty + stages;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.done + 1);
+  s.abort_flag = s.tmem_slot + 1;
+  s.bias_s = reinterpret_cast<float*>(s.abort_flag + 2);
+  s.masks = reinterpret_cast<uint32_t*>(s.bias_s + E32);
+  s.red = reinterpret_cast<float*>(s.masks + 4 * E32);
+  return s;
+}
+
+__global__ void __launch_bounds__(kTileTokens)
+    route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
+                      const __grid_constant__ CUtensorMap tm_gate, RouteArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_up_1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tile = blockIdx.x;
+  const int S = a.stages;
+  const int E32 = (a.E_pad + 31) & ~31;
+  const uint32_t a_bytes = kTileTokens * kBlockK * 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(a.E_pad) * kBlockK * 2;
+  const uint32_t stage_bytes = a_bytes + b_bytes;
+  RouteSmem sm = carve_route_smem(smem + static_cast<size_t>(S) * stage_bytes, S, E32);
+  const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(a.E_pad));
+
+  if (tile == 0 && tid == 0) *a.ticket = 0u;
+  if (warp == 0) {
+    tmem_alloc(sm.tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(sm.done, 1);
+    *sm.abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 2 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_gate);
+  }
+  for (int i = tid; i < E32; i += kTileTokens)
+    sm.bias_s[i] = (a.bias != nullptr && i < a.E) ? a.bias[i] : 0.f;
+  for (int i = tid; i < 4 * E32; i += kTileTokens) sm.masks[i] = 0u;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_slot;
+  const WaitCtl wc{sm.abort_flag, a.dev_status, a.timeout_ns};
+  const int nk = a.H / kBlockK;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    int kb = 0;
+    for (; kb < nk; ++kb) {
+      const int s = kb % S;
+      if (kb >= S && !mbar_wait(&sm.empty[s], ((kb / S) - 1) & 1, wc)) break;
+      uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+      mbar_arrive_expect_tx(&sm.full[s], stage_bytes);
+      tma_load_2d(st, &tm_x, &sm.full[s], kb * kBlockK, tile * kTileTokens);
+      tma_load_2d(st + a_bytes, &tm_gate, &sm.full[s], kb * kBlockK, 0);
+    }
+    if (kb < nk) {
+      // aborted: let the loads already issued land before the CTA exits
+      for (int d = (kb > S ? kb - S : 0); d < kb; ++d)
+        mbar_wait_drain(&sm.full[d % S], (d / S) & 1, 100000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // UMMA issuer: D[128 x E_pad] += X[128 x 64] * gate^T[64 x E_pad] per stage
+    const uint32_t idesc = idesc_bf16_f32(kTileTokens, static_cast<uint32_t>(a.E_pad), false, false);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % S;
+      if (!mbar_wait(&sm.full[s], (kb / S) & 1, wc)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
+      const uint32_t b_addr = a_addr + a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk) {
+        const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
+        const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
+        umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit(&sm.empty[s]);
+    }
+    umma_commit(sm.done);
+  }
+  __syncwarp();
+
+  // all threads: wait for the accumulator, then the routing epilogue (the
+  // decision is made CTA-uniform because the epilogue synchronises)
+  const bool done_ok = mbar_wait_drain(sm.done, 0, 4ull * a.timeout_ns);
+  const int go = __syncthreads_and(done_ok && *sm.abort_flag == 0u);
+  tc_fence_after();
+  if (go) {
+    TmemSource src{tmem + (static_cast<uint32_t>(32 * warp) << 16), sm.bias_s};
+    route_epilogue(src, a, tile, sm.masks, sm.red, E32);
+  } else if (tid == 0) {
+    atomicOr(a.dev_status, MOE_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+__global__ void __launch_bounds__(kTileTokens) route_logits_kernel(RouteArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x;
+  const int E32 = (a.E + 31) & ~31;
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw);
+  float* red = reinterpret_cast<float*>(masks + 4 * E32);
+  if (tile == 0 && tid == 0) *a.ticket = 0u;
+  for (int i = tid; i < 4 * E32; i += kTileTokens) masks[i] = 0u;
+  __syncthreads();
+  const int t = tile * kTileTokens + tid;
+  GlobalSource src{a.logits_in + static_cast<size_t>(t < a.T ? t : 0) * a.E, a.E, t < a.T};
+  route_epilogue(src, a, tile, masks, red, E32);
+}
+
+// Tile counts and ranks from caller-given indices. A slot is unusable if its
+// expert is outside [0,E) or repeats an earlier slot of the same token; the
+// gather kernel applies the same rule and drops it.
+__global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x;
+  const int E32 = (a.E + 31) & ~31;
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw);
+  if (tile == 0 && tid == 0) *a.ticket = 0u;
+  for (int i = tid; i < 4 * E32; i += kTileTokens) masks[i] = 0u;
+  __syncthreads();
+  const int t = tile * kTileTokens + tid;
+  const bool valid = t < a.T;
+  int e[kMaxTopK];
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    e[j] = -1;
+    if (valid && j < a.k) {
+      const int v = a.topk_idx[static_cast<size_t>(t) * a.k + j];
+      bool ok = v >= 0 && v < a.E;
+      if (!ok) bits |= MOE_DEV_BAD_INDEX;
+#pragma unroll
+      for (int jj = 0; jj < j; ++jj)
+        if (ok && e[jj] == v) {
+          ok = false;
+          bits |= MOE_DEV_DUP_INDEX;
+        }
+      e[j] = ok ? v : -1;
+    }
+  }
+  if (bits) atomicOr(a.dev_status, bits);
+  int rank[kMaxTopK];
+  tile_ranks(masks, E32, a.E, a.k, e, valid, rank, a.tile_cnt, a.n_tiles, tile);
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < a.k) a.rank8[static_cast<size_t>(t) * a.k + j] = static_cast<uint8_t>(rank[j]);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host ----
+
+int route_stages(int E_pad) {
+  const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
+  int s = (96 * 1024) / stage;
+  return s < 2 ? 2 : (s > 4 ? 4 : s);
+}
+
+size_t route_smem_bytes(int E_pad, int stages) {
+  const int E32 = (E_pad + 31) & ~31;
+  const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(E_pad) * kBlockK * 2;
+  return 1024 + stage * stages + 8 * (2 * stages + 1) + 16 + 4 * E32 + 2 * 4 * 4 * E32;
+}
+
+cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, int E, int E_pad,
+                                  cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(H) * E_pad;
+  int blocks = static_cast<int>((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  gate_transpose_kernel<<<blocks, 256, 0, st>>>(gate, gateT, H, E, E_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                              const RouteArgs& a, cudaStream_t st) {
+  const size_t smem = route_smem_bytes(a.E_pad, a.stages);
+  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  route_gemm_kernel<<<a.n_tiles, kTileTokens, smem, st>>>(tm_x, tm_gate, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
+  const int E32 = (a.E + 31) & ~31;
+  const size_t smem = 2 * 4 * 4 * static_cast<size_t>(E32);
+  route_logits_kernel<<<a.n_tiles, kTileTokens, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rank(const RankArgs& a, cudaStream_t st) {
+  const int E32 = (a.E + 31) & ~31;
+  rank_kernel<<<a.n_tiles, kTileTokens, 4 * 4 * E32, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
