@@ -246,7 +246,8 @@ def test_permute_empty_input():
 
 # ============================================================ expert FFN ==
 
-def _ffn_case(E, H, h, counts, k=2, seed=0):
+def _ffn_case(E, H, h, counts, seed=0):
+    k = min(2, E)
     counts = np.asarray(counts)
     N = int(counts.sum())
     T = max((N + k - 1) // k, 1)
@@ -281,7 +282,7 @@ def _ffn_gpu(s, xp, off, W1, W2):
 ])
 def test_expert_ffn_against_oracle(E, H, h, counts):
     T, N, xp, W1, W2, off = _ffn_case(E, H, h, counts, seed=E + H)
-    s = _shape(T, H, E, 2, h, 1.0)
+    s = _shape(T, H, E, min(2, E), h, 1.0)
     act, yp, st = _ffn_gpu(s, xp, off, W1, W2)
     assert st == 0
     x64 = np64(xp[:N])
@@ -317,10 +318,13 @@ def test_combine_against_oracle(T, H, k, drop):
     torch.cuda.synchronize()
     d = O.Dispatch(C=0, pos=None, kept_counts=None, offsets=None, dest_row=dest.numpy(),
                    src_token=None, N=N)
-    ref = O.combine(np64(yp), d, w.numpy().astype(np.float64), H)
+    w64 = w.numpy().astype(np.float64)
+    ref = O.combine(np64(yp), d, w64, H)
     got = np64(y.cpu())
-    # fp32 vs float64 accumulation: at most one bf16 step apart
-    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30).all()
+    # fp32 accumulation vs float64: one bf16 step of the result plus the
+    # fp32 rounding of the terms (which matters where terms cancel)
+    mag = O.combine(np.abs(np64(yp)), d, np.abs(w64), H)
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + mag * 2.0 ** -20).all()
     assert np.mean(got == ref) > 0.98
     assert (got[(dest.numpy() < 0).all(axis=1)] == 0).all()
 

@@ -18,9 +18,10 @@ namespace {
 
 // ----------------------------------------------------------- top-k list ----
 
-// A descending list of the k best (logit, expert) pairs in registers. A new
-// pair displaces an entry only if its logit is strictly larger, so among
-// equal logits the lower expert index (seen first) stays ahead.
+// A list of the k best (logit, expert) pairs in registers, ordered by
+// descending logit and, among equal logits, ascending expert index. An
+// inserted pair sinks past every entry that precedes it in that order; a
+// displaced entry carries on down the list the same way.
 struct TopK {
   float v[kMaxTopK];
   int i[kMaxTopK];
@@ -35,7 +36,7 @@ struct TopK {
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j < k) {
-        const bool gt = cv > v[j];
+        const bool gt = cv > v[j] || (cv == v[j] && ce < i[j]);
         const float ov = v[j];
         const int oi = i[j];
         v[j] = gt ? cv : ov;
