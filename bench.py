@@ -153,6 +153,11 @@ def run_ours(args, rank, world, local_rank):
     for row in ev:
         for e in row:
             e.record(stream)
+    # inputs re-read every step; below 2x L2 they could stay cached, so then
+    # L2 is flushed between steps and each step is timed by its own events
+    in_bytes = sum(v.numel() * v.element_size() for v in d.values() if v is not None)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) \
+        if in_bytes < 2 * L2_BYTES else None
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     torch.cuda.synchronize(dev)
@@ -162,13 +167,18 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     t0.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(float(i))
         step(ev[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
+    if flush is None:
+        ms = t0.elapsed_time(t1) / args.steps
+    else:
+        ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)) / args.steps
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -179,10 +189,21 @@ def run_ours(args, rank, world, local_rank):
     n_kept = int(offsets[E].item())
     any_kept = int((dest >= 0).any(dim=1).sum().item())
 
-    # end to end through the public API with host buffers: copy x in, read y
-    # and aux out, every step, inside the timed region
+    e2e = None if args.no_e2e else run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
+    if rank != 0:
+        return None
+    l2 = (f"L2 flushed between steps ({2 * L2_BYTES >> 20} MB write); steps timed by their own events"
+          if flush is not None else
+          f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB re-read per step); no flush")
+    return report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2)
+
+
+def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
+    """End to end through the public API with host buffers: copy x in, read
+    y and aux out, every step, inside the timed region."""
+    T, H = inp["x"].shape
     x_host = inp["x"].pin_memory()
-    y_host = torch.empty((T, w.H), dtype=torch.bfloat16).pin_memory()
+    y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
     x_dev = torch.empty_like(d["x"])
 
@@ -209,9 +230,11 @@ def run_ours(args, rank, world, local_rank):
         tt = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
+    return {"ms": e2e_ms, "h2d": T * H * 2, "d2h": T * H * 2 + 4}
 
-    if rank != 0:
-        return None
+
+def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2):
+    T, k = w.T, w.k
     pk = peaks()
     work = algorithmic_work(w, n_kept, any_kept)
     names = ["route", "scan", "permute", "gemm1", "gemm2", "combine"]
@@ -243,11 +266,12 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "parallelism": f"replicas x{world} (no exchange)",
-                   "l2": "inputs larger than L2 (x 268 MB, W1/W2 1.9 GB each); no flush"},
+                   "l2": l2},
         "clocks": clk,
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": T * w.H * 2,
-                "d2h_bytes_per_step": T * w.H * 2 + 4},
+        "e2e": None if e2e is None else {
+            "value": round(tokens / (e2e["ms"] / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
+            "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": 7 * args.steps,
         "roofline": roofline,
         "kernels": kern,
@@ -319,12 +343,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=W.WORKLOAD_ORDER + list(W.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

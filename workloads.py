@@ -64,6 +64,13 @@ WORKLOADS = {
                             "normal1.5",
                             note="random bias idles about 30% of the experts"),
 }
+# A small case of the large-expert layer's expert FFN for profiler captures:
+# the same K, N and tile shapes (H=4096, h=14336), two experts of 4096 rows,
+# weights (235 MB each) still larger than L2, under 1 GB on the device.
+PROFILE_WORKLOADS = {
+    "ffn_profile": Workload("ffn_profile", 4096, 4096, 2, 2, 14336, 1.25,
+                            note="profiler capture case of the large-expert FFN"),
+}
 # Positional aliases, in the order the workloads are usually listed.
 WORKLOAD_ORDER = ["tiny", "imbalanced", "large_expert", "fine_grained", "many_expert"]
 
@@ -71,6 +78,8 @@ WORKLOAD_ORDER = ["tiny", "imbalanced", "large_expert", "fine_grained", "many_ex
 def get(name_or_index) -> Workload:
     if isinstance(name_or_index, int):
         return WORKLOADS[WORKLOAD_ORDER[name_or_index - 1]]
+    if name_or_index in PROFILE_WORKLOADS:
+        return PROFILE_WORKLOADS[name_or_index]
     return WORKLOADS[name_or_index]
 
 
