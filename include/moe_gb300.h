@@ -173,6 +173,24 @@ moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* 
                          int32_t* offsets, int32_t* dest_row, uint32_t* dev_status,
                          void* ws, size_t ws_bytes, void* stream, void* const* events);
 
+/* moe_permute for callers that cannot allocate device memory. The pages
+ * have no counterpart to this entry point; it serves code that may not call
+ * cudaMalloc or hold a workspace: a plugin inside a runtime that owns all
+ * device memory, or code issuing work while a stream is being captured.
+ * Same arguments and results as moe_permute, minus ws/ws_bytes: the scratch
+ * is one static 1 MiB device array per GPU, held until the process exits.
+ *   - Shapes whose scratch exceeds 1 MiB (2 * E * ceil(T/128) * 4 bytes of
+ *     tile counters plus T*k rank bytes, each rounded up to 256, plus 1 KiB)
+ *     return MOE_ERR_UNSUPPORTED before any launch.
+ *   - The first call on a device looks the array's address up (once per
+ *     device); make it before any stream capture.
+ *   - All calls on a device share the array; calls that overlap on the GPU
+ *     race and must be serialised by the caller. Allocates nothing. */
+moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+                               int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                               int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

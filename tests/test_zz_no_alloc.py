@@ -1,0 +1,66 @@
+"""The workspace-free dispatch entry point, for callers that cannot allocate
+device memory (a plugin in a runtime that owns all device memory, or code
+running while a stream is captured). Its scratch is a static device array
+inside the library; this checks it against moe_permute with a caller
+workspace, bit for bit, over two calls in a row (the second call must not
+see the first call's leftovers). Collected last on purpose."""
+import numpy as np
+import pytest
+import torch
+
+import top_routing_expert_gb300 as moe
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.build()
+    moe.load_library()
+
+
+def _outputs(T, H, E, k):
+    z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=DEV)
+    return dict(kept_counts=z(E, torch.int32), offsets=z(E + 1, torch.int32),
+                dest_row=z((T, k), torch.int32),
+                src_token=torch.full((T * k,), -1, dtype=torch.int32, device=DEV),
+                x_perm=z((T * k, H), torch.bfloat16), dev_status=z(1, torch.int32))
+
+
+def _compare(a, b):
+    n = int(a["offsets"][-1].item())
+    assert torch.equal(a["kept_counts"], b["kept_counts"])
+    assert torch.equal(a["offsets"], b["offsets"])
+    assert torch.equal(a["dest_row"], b["dest_row"])
+    assert torch.equal(a["src_token"][:n], b["src_token"][:n])
+    assert torch.equal(a["x_perm"][:n].view(torch.int16), b["x_perm"][:n].view(torch.int16))
+    assert int(a["dev_status"].item()) == int(b["dev_status"].item()) == 0
+
+
+def test_noalloc_permute_matches_workspace_permute_twice_in_a_row():
+    cases = [(1000, 192, 12, 3, 1.0, 0.4, 1),   # ragged, drops
+             (4096, 256, 16, 2, 1.0, 0.9, 2)]   # heavy skew, other sizes
+    for T, H, E, k, cf, skew, seed in cases:
+        s = moe.MoeShape.make(T, H, E, k, 64, cf)
+        x = W.make_inputs(W.custom(T, H, E, k, 64, cf), seed=seed, with_weights=False)["x"].to(DEV)
+        idx = W.make_topk_idx(T, E, k, seed=seed, skew=skew).to(DEV)
+        ref = _outputs(T, H, E, k)
+        moe.moe_permute(s, x, idx, ws=moe.Workspace(s), **ref)
+        got = _outputs(T, H, E, k)
+        moe.moe_permute_noalloc(s, x, idx, **got)
+        torch.cuda.synchronize()
+        _compare(ref, got)
+
+
+def test_noalloc_rejects_shapes_beyond_its_static_scratch():
+    s = moe.MoeShape.make(131072, 64, 128, 2, 64, 1.1)   # needs > 1 MiB of scratch
+    one_i = torch.zeros((1, 2), dtype=torch.int32, device=DEV)
+    one_x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
+    offs = torch.zeros(129, dtype=torch.int32, device=DEV)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_permute_noalloc(s, one_x, one_i, None, offs, one_i, None, one_x)
+    assert e.value.code == 3

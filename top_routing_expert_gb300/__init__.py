@@ -20,7 +20,7 @@ from ._build import LIB, build  # noqa: F401  (re-exported)
 __all__ = [
     "MoeError", "MoeShape", "load_library", "capacity", "workspace_size", "status_str",
     "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
-    "moe_combine", "moe_layer_fwd", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
+    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
 
@@ -28,7 +28,7 @@ DEV_BAD_INDEX, DEV_DUP_INDEX, DEV_NONFINITE, DEV_TIMEOUT = 1, 2, 4, 8
 LAYER_NUM_EVENTS = 7
 EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "moe_status_str",
                     "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
-                    "moe_combine", "moe_layer_fwd"]
+                    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -80,6 +80,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_combine.argtypes = [S] + [_P] * 5
     lib.moe_layer_fwd.restype = ctypes.c_int
     lib.moe_layer_fwd.argtypes = [S] + [_P] * 16 + [ctypes.c_size_t, _P, _P]
+    lib.moe_permute_noalloc.restype = ctypes.c_int
+    lib.moe_permute_noalloc.argtypes = [S] + [_P] * 9
     _lib = lib
     return lib
 
@@ -234,3 +236,19 @@ def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None,
         _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
         _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
+
+
+def moe_permute_noalloc(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x_perm,
+                        dev_status=None, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate
+    device memory: its scratch is a static 1 MiB device array inside the
+    library (one per GPU). Larger shapes raise MoeError (unsupported).
+    Calls that overlap on the GPU share that array and must be serialised;
+    make the first call on a device before any stream capture."""
+    s = _shape(shape)
+    _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
+        _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        _stream(stream)))
