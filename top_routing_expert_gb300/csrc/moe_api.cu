@@ -184,7 +184,8 @@ EncodeTiledFn encode_fn() {
 // A bf16 row-major matrix [outer, inner] read in boxes of box_outer rows x
 // box_inner (= 64, one 128-byte swizzle row) columns.
 bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                  uint32_t box_inner, uint32_t box_outer) {
+                  uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t gdim[2] = {inner, outer};
@@ -192,7 +193,7 @@ bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estride[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box,
-            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -239,10 +240,13 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
     MOE_CUDA(launch_route_logits(a, st));
   } else {
     MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
-    CUtensorMap tm_x, tm_g;
+    CUtensorMap tm_x, tm_g, tm_rows;
     if (!tmap_bf16_2d(&tm_x, x, d.H, d.T, kBlockK, kTileTokens)) return MOE_ERR_CUDA;
     if (!tmap_bf16_2d(&tm_g, w.gateT, d.H, d.E_pad, kBlockK, d.E_pad)) return MOE_ERR_CUDA;
-    MOE_CUDA(launch_route_gemm(tm_x, tm_g, a, st));
+    // 256-column row pieces (512 B), used only for L2 prefetch
+    if (!tmap_bf16_2d(&tm_rows, x, d.H, d.T, 256, kTileTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+    MOE_CUDA(launch_route_gemm(tm_x, tm_g, tm_rows, a, st));
   }
   return MOE_OK;
 }

@@ -178,9 +178,11 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
   }
 }
 
-// One warp per token; slots accumulate in ascending j, fp32.
-template <int U>
-__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+// One warp per token; slots accumulate in ascending j, fp32. Every kept
+// slot's vectors are loaded before any is used, so a token's k row reads are
+// in flight together.
+template <int KMAX, int U>
+__global__ void __launch_bounds__(256, 3) combine_kernel(CombineArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 3;
@@ -195,32 +197,35 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
       wl = a.topk_w[static_cast<size_t>(t) * a.k + lane];
       if (dl < 0 || dl >= rows) dl = -1;  // only rows of the buffer are read
     }
-    int d[kMaxTopK];
-    float w[kMaxTopK];
+    int d[KMAX];
+    float w[KMAX];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       d[j] = __shfl_sync(0xffffffffu, dl, j);
       w[j] = __shfl_sync(0xffffffffu, wl, j);
+      if (j >= a.k) d[j] = -1;
     }
     for (int b = 0; b < nvec; b += 32 * U) {
+      uint4 v[KMAX][U];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = b + 32 * u + lane;
+          v[j][u] = (d[j] >= 0 && i < nvec) ? __ldg(yv + static_cast<size_t>(d[j]) * nvec + i)
+                                           : make_uint4(0, 0, 0, 0);
+        }
       float acc[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < a.k && d[j] >= 0) {
-          const uint4* src = yv + static_cast<size_t>(d[j]) * nvec;
-          uint4 v[U];
+      for (int j = 0; j < KMAX; ++j) {
+        if (d[j] >= 0) {
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const int i = b + 32 * u + lane;
-            v[u] = i < nvec ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            const uint32_t wd[4] = {v[j][u].x, v[j][u].y, v[j][u].z, v[j][u].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               acc[u][2 * q] = fmaf(w[j], bf16_lo(wd[q]), acc[u][2 * q]);
@@ -269,11 +274,11 @@ cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   const int grid = warp_grid(a.T, num_sms);
   if (a.k <= 2)
-    combine_kernel<4><<<grid, 256, 0, st>>>(a);
+    combine_kernel<2, 4><<<grid, 256, 0, st>>>(a);
   else if (a.k <= 4)
-    combine_kernel<2><<<grid, 256, 0, st>>>(a);
+    combine_kernel<4, 2><<<grid, 256, 0, st>>>(a);
   else
-    combine_kernel<1><<<grid, 256, 0, st>>>(a);
+    combine_kernel<8, 1><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,25 +16,29 @@ namespace moe {
 
 namespace {
 
+constexpr int kRowGroup = 4;           // k-blocks per 512-byte row prefetch
+constexpr int kRouteGroupsAhead = 2;   // row prefetches in flight ahead of the loads
+
 // ----------------------------------------------------------- top-k list ----
 
 // A list of the k best (logit, expert) pairs in registers, ordered by
 // descending logit and, among equal logits, ascending expert index. An
 // inserted pair sinks past every entry that precedes it in that order; a
 // displaced entry carries on down the list the same way.
+template <int KMAX>
 struct TopK {
-  float v[kMaxTopK];
-  int i[kMaxTopK];
+  float v[KMAX];
+  int i[KMAX];
   __device__ __forceinline__ void init() {
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       v[j] = -INFINITY;
       i[j] = -1;
     }
   }
   __device__ __forceinline__ void insert(float cv, int ce, int k) {
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         const bool gt = cv > v[j] || (cv == v[j] && ce < i[j]);
         const float ov = v[j];
@@ -55,20 +59,21 @@ struct TopK {
 // slot the number of earlier tokens of the tile that chose the same expert
 // (warp bit masks in shared memory, OR-ed, so the result does not depend on
 // thread timing) and writes the tile's per-expert counts.
+template <int KMAX>
 __device__ __forceinline__ void tile_ranks(uint32_t* masks, int E_stride, int E, int k,
-                                           const int (&e)[kMaxTopK], bool row_valid,
-                                           int (&rank)[kMaxTopK], int32_t* tile_cnt,
+                                           const int (&e)[KMAX], bool row_valid,
+                                           int (&rank)[KMAX], int32_t* tile_cnt,
                                            int n_tiles, int tile) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (row_valid) {
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
+    for (int j = 0; j < KMAX; ++j)
       if (j < k && e[j] >= 0) atomicOr(&masks[warp * E_stride + e[j]], 1u << lane);
   }
   __syncthreads();
   const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     rank[j] = 0;
     if (j < k && row_valid && e[j] >= 0) {
       int r = __popc(masks[warp * E_stride + e[j]] & below);
@@ -115,7 +120,7 @@ struct GlobalSource {
 
 // The routing epilogue shared by both paths; identical arithmetic, so equal
 // logits give bit-identical results. All 128 threads call it.
-template <class Src>
+template <int KMAX, class Src>
 __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
                                                uint32_t* masks, float* red, int E_stride) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -125,7 +130,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
   const int nchunks = (E + 31) / 32;
 
   // pass 1: top-k on the logits (its first entry is the max), finiteness
-  TopK tk;
+  TopK<KMAX> tk;
   tk.init();
   bool bad = false;
   float* lrow = (a.logits_out && valid) ? a.logits_out + static_cast<size_t>(t) * E : nullptr;
@@ -173,21 +178,21 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
   }
 
   // renormalised top-k weights: p_j / sum_j' p_j' = ex_j / sum ex_j'
-  float ex[kMaxTopK];
+  float ex[KMAX];
   float den = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     ex[j] = (j < k && tk.i[j] >= 0) ? expf(tk.v[j] - m) : 0.f;
     den += ex[j];
   }
 
-  int rank[kMaxTopK];
+  int rank[KMAX];
   tile_ranks(masks, E_stride, E, k, tk.i, valid, rank, a.tile_cnt, a.n_tiles, tile);
 
   if (valid) {
     const size_t base = static_cast<size_t>(t) * k;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         a.topk_idx[base + j] = tk.i[j];
         a.topk_w[base + j] = ex[j] / den;
@@ -244,9 +249,11 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
   return s;
 }
 
+template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
-                      const __grid_constant__ CUtensorMap tm_gate, RouteArgs a) {
+                      const __grid_constant__ CUtensorMap tm_gate,
+                      const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -288,7 +295,13 @@ __global__ void __launch_bounds__(kTileTokens)
   const int nk = a.H / kBlockK;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // TMA producer. The swizzled loads read 128-byte pieces of rows that lie
+    // H*2 bytes apart; ahead of them, L2 prefetches through a plain (no
+    // swizzle) map fetch 512 contiguous bytes of each of the tile's rows, so
+    // DRAM sees whole row segments instead of scattered 128-byte pieces.
+    const int n_groups = (nk + kRowGroup - 1) / kRowGroup;
+    for (int g = 0; g < kRouteGroupsAhead && g < n_groups; ++g)
+      tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
     int kb = 0;
     for (; kb < nk; ++kb) {
       const int s = kb % S;
@@ -297,6 +310,11 @@ __global__ void __launch_bounds__(kTileTokens)
       mbar_arrive_expect_tx(&sm.full[s], stage_bytes);
       tma_load_2d(st, &tm_x, &sm.full[s], kb * kBlockK, tile * kTileTokens);
       tma_load_2d(st + a_bytes, &tm_gate, &sm.full[s], kb * kBlockK, 0);
+      if (kb % kRowGroup == 0) {
+        const int g = kb / kRowGroup + kRouteGroupsAhead;
+        if (g < n_groups)
+          tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
+      }
     }
     if (kb < nk) {
       // aborted: let the loads already issued land before the CTA exits
@@ -331,7 +349,7 @@ __global__ void __launch_bounds__(kTileTokens)
   tc_fence_after();
   if (go) {
     TmemSource src{tmem + (static_cast<uint32_t>(32 * warp) << 16), sm.bias_s};
-    route_epilogue(src, a, tile, sm.masks, sm.red, E32);
+    route_epilogue<KMAX>(src, a, tile, sm.masks, sm.red, E32);
   } else if (tid == 0) {
     atomicOr(a.dev_status, MOE_DEV_TIMEOUT);
   }
@@ -340,6 +358,7 @@ __global__ void __launch_bounds__(kTileTokens)
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
+template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens) route_logits_kernel(RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x;
@@ -352,7 +371,7 @@ __global__ void __launch_bounds__(kTileTokens) route_logits_kernel(RouteArgs a) 
   __syncthreads();
   const int t = tile * kTileTokens + tid;
   GlobalSource src{a.logits_in + static_cast<size_t>(t < a.T ? t : 0) * a.E, a.E, t < a.T};
-  route_epilogue(src, a, tile, masks, red, E32);
+  route_epilogue<KMAX>(src, a, tile, masks, red, E32);
 }
 
 // Tile counts and ranks from caller-given indices. A slot is unusable if its
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
   }
   if (bits) atomicOr(a.dev_status, bits);
   int rank[kMaxTopK];
-  tile_ranks(masks, E32, a.E, a.k, e, valid, rank, a.tile_cnt, a.n_tiles, tile);
+  tile_ranks<kMaxTopK>(masks, E32, a.E, a.k, e, valid, rank, a.tile_cnt, a.n_tiles, tile);
   if (valid) {
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
@@ -402,9 +421,10 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 // ------------------------------------------------------------------ host ----
 
 int route_stages(int E_pad) {
+  // as many stages as fit in ~108 KB, so that two CTAs share an SM
   const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
-  int s = (96 * 1024) / stage;
-  return s < 2 ? 2 : (s > 4 ? 4 : s);
+  int s = (108 * 1024) / stage;
+  return s < 2 ? 2 : (s > 6 ? 6 : s);
 }
 
 size_t route_smem_bytes(int E_pad, int stages) {
@@ -422,21 +442,34 @@ cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                              const RouteArgs& a, cudaStream_t st) {
+template <int KMAX>
+cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                                const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
   const size_t smem = route_smem_bytes(a.E_pad, a.stages);
-  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel,
+  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  route_gemm_kernel<<<a.n_tiles, kTileTokens, smem, st>>>(tm_x, tm_gate, a);
+  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens, smem, st>>>(tm_x, tm_gate, tm_x_rows, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+  if (a.k <= 2) return launch_route_gemm_k<2>(tm_x, tm_gate, tm_x_rows, a, st);
+  if (a.k <= 4) return launch_route_gemm_k<4>(tm_x, tm_gate, tm_x_rows, a, st);
+  return launch_route_gemm_k<8>(tm_x, tm_gate, tm_x_rows, a, st);
 }
 
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
   const int E32 = (a.E + 31) & ~31;
   const size_t smem = 2 * 4 * 4 * static_cast<size_t>(E32);
-  route_logits_kernel<<<a.n_tiles, kTileTokens, smem, st>>>(a);
+  if (a.k <= 2)
+    route_logits_kernel<2><<<a.n_tiles, kTileTokens, smem, st>>>(a);
+  else if (a.k <= 4)
+    route_logits_kernel<4><<<a.n_tiles, kTileTokens, smem, st>>>(a);
+  else
+    route_logits_kernel<8><<<a.n_tiles, kTileTokens, smem, st>>>(a);
   return cudaGetLastError();
 }
 
