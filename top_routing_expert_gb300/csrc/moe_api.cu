@@ -160,6 +160,14 @@ uint64_t wait_timeout_ns() {
   return v;
 }
 
+bool use_pair_gemm() {
+  static const bool v = [] {
+    const char* e = getenv("MOE_GB300_GEMM");
+    return e != nullptr && strcmp(e, "pair") == 0;
+  }();
+  return v;
+}
+
 // ------------------------------------------------------------ TMA maps ----
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -311,7 +319,10 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.gelu = gelu;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
-  MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));
+  if (use_pair_gemm())
+    MOE_CUDA(launch_grouped_gemm_pair(tm_a, tm_b, g, num_sms(), st));
+  else
+    MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));
   return MOE_OK;
 }
 

@@ -1,0 +1,329 @@
+// Grouped GEMM over ragged expert segments, CTA-pair version: the same
+// product as grouped_gemm_kernel (D[r,:] = A[r,:] . B[e(r)], optional GELU)
+// with a 2-CTA UMMA (cta_group::2, M=256, N=256). Each CTA of a cluster pair
+// holds its own 128 rows of A and its own 128 columns of B per stage, so a
+// stage is 32 KB instead of 48 KB: six stages fit, and shared memory moves
+// a third less data per FLOP than the single-CTA kernel.
+//
+// A pair tile is (expert e, pair index pm, n-tile): CTA rank r computes the
+// expert's local m-tile 2*pm + r (128 rows) against all 256 columns. An
+// expert with an odd m-tile count leaves the last pair's second half past
+// the segment end; its rows are computed and never stored.
+//
+// Roles per CTA (192 threads): warp 0 = TMA producer (both CTAs, own halves,
+// transaction bytes counted on the leader's barrier); warp 1 = UMMA issuer
+// (leader only) and TMEM allocation (both, collectively); warps 2-5 =
+// epilogue of the CTA's own 128 rows. Stage and accumulator barriers are
+// released to both CTAs by multicast commits; the leader waits for both
+// epilogues before reusing an accumulator.
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBM = 128;           // rows per CTA; the pair computes 256
+constexpr int kBN = 256;           // columns per pair tile (128 held by each CTA)
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kBM * kBlockK * 2;          // 16 KB
+constexpr uint32_t kBBytes = (kBN / 2) * kBlockK * 2;    // 16 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 32 KB
+constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
+constexpr int kGroupPairs = 8;                           // pair m-tiles per raster group
+
+struct PairTile {
+  int e, row0, row_end, n0;
+};
+
+__device__ __forceinline__ PairTile decode_pair(int L, const int* pm_prefix, const int* offs,
+                                                int E, int total_pm, int n_tiles_n, int rank) {
+  const int per_group = kGroupPairs * n_tiles_n;
+  const int g = L / per_group;
+  const int first = g * kGroupPairs;
+  const int gsz = min(kGroupPairs, total_pm - first);
+  const int r = L - g * per_group;
+  const int pm = first + r % gsz;
+  const int nt = r / gsz;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pm_prefix[mid] <= pm) lo = mid; else hi = mid - 1;
+  }
+  PairTile t;
+  t.e = lo;
+  t.row0 = offs[lo] + (2 * (pm - pm_prefix[lo]) + rank) * kBM;
+  t.row_end = offs[lo + 1];
+  t.n0 = nt * kBN;
+  return t;
+}
+
+__device__ __forceinline__ float gelu_tanh_f(float u) {
+  // 0.5 u (1 + tanh(z)) = u / (1 + exp(-2 z)),  z = sqrt(2/pi) (u + 0.044715 u^3)
+  const float z2 = 1.5957691216057308f * fmaf(0.044715f * u, u * u, u);
+  return __fdividef(u, 1.0f + __expf(-z2));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
+                             const __grid_constant__ CUtensorMap tm_b, GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_up_1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* abort_flag = tmem_slot + 1;
+  int* offs = reinterpret_cast<int*>(abort_flag + 2);  // [E+1]
+  int* pm_prefix = offs + (p.E + 1);                    // [E+1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  for (int i = tid; i <= E; i += kThreads) {
+    const int v = p.offsets[i];
+    offs[i] = v < 0 ? 0 : (v > p.rows ? p.rows : v);  // rows outside the buffer are never written
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 2 && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * 4 * 32);  // both CTAs' epilogue threads
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 3 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int i = 1; i <= E; ++i) offs[i] = offs[i] < offs[i - 1] ? offs[i - 1] : offs[i];
+  __syncthreads();
+  if (warp == 0) {
+    // pair m-tiles per expert (ceil of half its 128-row m-tiles), prefix
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int mt = e < E ? (offs[e + 1] - offs[e] + kBM - 1) / kBM : 0;
+      const int pm = (mt + 1) >> 1;
+      int incl = pm;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) pm_prefix[e] = carry + incl - pm;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pm_prefix[E] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barrier initialisation visible to the peer before any remote use
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_pm = pm_prefix[E];
+  const int n_tiles_n = (p.N + kBN - 1) / kBN;
+  const int total = total_pm * n_tiles_n;
+  const int nk = p.K / kBlockK;
+  const WaitCtl wc{abort_flag, p.dev_status, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer ----
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool aborted = false;
+      for (int L = cluster; L < total && !aborted; L += n_clusters) {
+        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+        const int b_row = c.e * p.K;
+        const int b_col = c.n0 + static_cast<int>(rank) * (kBN / 2);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+          uint8_t* sa = smem + stage * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          tma_load_2d_pair(sa, &tm_a, bar, kb * kBlockK, c.row0);
+#pragma unroll
+          for (int cb = 0; cb < kBN / 2 / 64; ++cb)
+            tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
+                             b_row + kb * kBlockK);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted && leader) {
+        // let the last loads issued land before the CTA exits
+        int s = stage;
+        uint32_t ph = phase;
+        for (int d = 0; d < kStages && d < issued; ++d) {
+          if (--s < 0) {
+            s = kStages - 1;
+            ph ^= 1u;
+          }
+          mbar_wait_drain(&full[s], ph, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------- UMMA issuer (leader) ----
+      const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, false, true);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool aborted = false;
+      for (int L = cluster; L < total && !aborted; L += n_clusters) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            // A: K-major 128-byte rows, 16-element K step = 32 bytes.
+            const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
+            // B: MN-major, one 128-byte row per k, 16-row K step = 2 KB,
+            // this CTA's two 64-column blocks 8 KB apart.
+            const uint64_t bd = smem_desc_sw128(b_addr + 2048u * kk, 64u * kBlockK * 2, 1024u);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        umma_commit_pair_multicast(&tfull[acc], 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every UMMA issued must finish before TMEM is released
+      umma_commit_pair(drain);
+      mbar_wait_drain(drain, 0, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------ epilogue ----
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
+                                       mapa_shared(smem_u32(&tempty[1]), 0)};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int L = cluster; L < total; L += n_clusters) {
+      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      tc_fence_after();
+      const int row = c.row0 + 32 * q + lane;
+      const bool valid = row < c.row_end;
+      uint16_t* drow = p.D + static_cast<size_t>(valid ? row : 0) * p.N;
+      const uint32_t t_base =
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        const int col = c.n0 + 32 * cc;
+        if (col >= p.N) break;  // N is a multiple of 64: whole chunks
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + 32u * cc, r);
+        tmem_ld_wait();
+        if (valid) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float v0 = __uint_as_float(r[2 * i]);
+            float v1 = __uint_as_float(r[2 * i + 1]);
+            if (p.gelu) {
+              v0 = gelu_tanh_f(v0);
+              v1 = gelu_tanh_f(v1);
+            }
+            packed[i] = pack_bf16x2(v0, v1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(drow + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(tempty_leader[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the peer may still signal it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace
+
+size_t gemm_pair_smem_bytes(int E) {
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 8 * (2 * kStages + 5) + 16 +
+         8 * static_cast<size_t>(E + 1);
+}
+
+cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const GemmArgs& a, int num_sms, cudaStream_t st) {
+  const size_t smem = gemm_pair_smem_bytes(a.E);
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, tm_a, tm_b, a);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

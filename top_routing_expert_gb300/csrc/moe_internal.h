@@ -110,5 +110,8 @@ cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const GemmArgs& a, int num_sms, cudaStream_t st);
+size_t gemm_pair_smem_bytes(int E);
 
 }  // namespace moe
