@@ -279,6 +279,9 @@ def _ffn_gpu(s, xp, off, W1, W2):
     (8, 256, 512, [160] * 8),                     # tiny workload, full capacity
     (16, 1024, 2816, [512, 512, 384, 300, 200, 150, 100, 90, 50, 30, 10, 5, 2, 1, 0, 0]),
     (64, 2048, 1408, list(np.random.default_rng(0).integers(0, 300, 64))),  # fine-grained shape
+    # >= 4096 rows: the CTA-pair kernel, with empty, 1-row and odd-m-tile segments
+    (6, 128, 192, [0, 1, 129, 4000, 257, 1]),
+    (3, 256, 320, [2048, 0, 2176]),
 ])
 def test_expert_ffn_against_oracle(E, H, h, counts):
     T, N, xp, W1, W2, off = _ffn_case(E, H, h, counts, seed=E + H)

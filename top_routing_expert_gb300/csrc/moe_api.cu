@@ -160,13 +160,10 @@ uint64_t wait_timeout_ns() {
   return v;
 }
 
-bool use_pair_gemm() {
-  static const bool v = [] {
-    const char* e = getenv("MOE_GB300_GEMM");
-    return e != nullptr && strcmp(e, "pair") == 0;
-  }();
-  return v;
-}
+// The CTA-pair grouped GEMM moves a third less shared-memory traffic per FLOP
+// and wins from a few thousand rows up; below that the single-CTA kernel's
+// finer 128-row tiles waste less on ragged segments.
+constexpr int64_t kPairGemmMinRows = 4096;
 
 // ------------------------------------------------------------ TMA maps ----
 
@@ -319,7 +316,7 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.gelu = gelu;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
-  if (use_pair_gemm())
+  if (d.A >= kPairGemmMinRows)
     MOE_CUDA(launch_grouped_gemm_pair(tm_a, tm_b, g, num_sms(), st));
   else
     MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));

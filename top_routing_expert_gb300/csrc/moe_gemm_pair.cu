@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool aborted = false;
+      const uint64_t pol_a = l2_policy_evict_last();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
         const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
         const int b_row = c.e * p.K;
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
-          tma_load_2d_pair(sa, &tm_a, bar, kb * kBlockK, c.row0);
+          // A rows are reused by every n-tile of the group: keep them in L2
+          tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kBlockK, c.row0, pol_a);
 #pragma unroll
           for (int cb = 0; cb < kBN / 2 / 64; ++cb)
             tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
@@ -272,10 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             packed[i] = pack_bf16x2(v0, v1);
           }
+          // outputs are read once, by the next kernel: stream them past L2
           uint4* dst = reinterpret_cast<uint4*>(drow + col);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                                packed[4 * i + 3]));
         }
       }
       tc_fence_before();

@@ -91,118 +91,169 @@ __device__ __forceinline__ void tile_ranks(uint32_t* masks, int E_stride, int E,
 
 // --------------------------------------------------------------- sources ----
 
-// Logits of the thread's row from TMEM (GEMM path), plus the gate bias.
+// Each epilogue thread owns one token row (TMEM lane) and one part of 32
+// expert columns of it: a CTA runs kTileTokens * NPART threads, warp w
+// reading lane quadrant w % 4 and part w / 4.
+constexpr int kCols = 32;
+
+// Logits of the thread's row and part from TMEM (GEMM path), plus the bias.
 struct TmemSource {
   uint32_t taddr;       // TMEM address of (this warp's lane quadrant, column 0)
-  const float* bias_s;  // shared, >= 32 * chunks entries, zero past E
-  __device__ __forceinline__ void load(int c, float (&v)[32]) const {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + 32u * c, r);
+  const float* bias_s;  // shared, zero past E
+  __device__ __forceinline__ void load(int part, float (&v)[kCols]) const {
+    uint32_t r[kCols];
+    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(kCols * part), r);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + bias_s[32 * c + i];
+    for (int i = 0; i < kCols; ++i) v[i] = __uint_as_float(r[i]) + bias_s[kCols * part + i];
   }
 };
 
-// Logits of the thread's row from global memory (logits entry point).
+// Logits of the thread's row and part from global memory (logits entry point).
 struct GlobalSource {
   const float* row;
   int E;
   bool valid;
-  __device__ __forceinline__ void load(int c, float (&v)[32]) const {
+  __device__ __forceinline__ void load(int part, float (&v)[kCols]) const {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = 32 * c + i;
+    for (int i = 0; i < kCols; ++i) {
+      const int e = kCols * part + i;
       v[i] = (valid && e < E) ? row[e] : 0.f;
     }
   }
 };
 
-// The routing epilogue shared by both paths; identical arithmetic, so equal
-// logits give bit-identical results. All 128 threads call it.
-template <int KMAX, class Src>
-__device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
-                                               uint32_t* masks, float* red, int E_stride) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int E = a.E, k = a.k;
-  const int t = tile * kTileTokens + tid;
-  const bool valid = t < a.T;
-  const int nchunks = (E + 31) / 32;
+// Shared scratch of the routing epilogue.
+template <int KMAX, int NPART>
+struct EpiSmem {
+  float cand_v[kTileTokens][NPART][KMAX];  // per-part top-k lists; part 0 ends merged
+  int cand_i[kTileTokens][NPART][KMAX];
+  float psum[kTileTokens][NPART];          // per-part softmax partial sums
+  float rowmax[kTileTokens];
+  float rowsum[kTileTokens];
+};
 
-  // pass 1: top-k on the logits (its first entry is the max), finiteness
+// The routing epilogue shared by both paths; identical arithmetic, so equal
+// logits give bit-identical results. All threads of the CTA call it.
+//   1. each thread: top-k of its 32 columns (ascending expert order);
+//   2. part 0 merges the parts' lists in part order -> the token's top-k and
+//      its max m (the order-defined comparator makes the merge exact);
+//   3. softmax denominator: per-part sums of exp(l - m), added in part order;
+//   4. weights exp(l_j - m) / sum_j exp(l_j - m) over the chosen k;
+//   5. in-tile arrival ranks and per-tile expert counts from warp bit masks;
+//   6. per-expert sums of p over the tile's tokens (fixed butterfly per warp,
+//      then quadrants in order).
+template <int KMAX, int NPART, class Src>
+__device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
+                                               EpiSmem<KMAX, NPART>& es, uint32_t* masks,
+                                               float* red, int E_stride) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = warp & 3, part = warp >> 2;
+  const int r = 32 * q + lane;
+  const int E = a.E, k = a.k;
+  const int t = tile * kTileTokens + r;
+  const bool valid = t < a.T;
+  const int c0 = kCols * part;
+
+  float v[kCols];
+  src.load(part, v);
   TopK<KMAX> tk;
   tk.init();
   bool bad = false;
   float* lrow = (a.logits_out && valid) ? a.logits_out + static_cast<size_t>(t) * E : nullptr;
-  for (int c = 0; c < nchunks; ++c) {
-    float v[32];
-    src.load(c, v);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = 32 * c + i;
-      if (e < E) {
-        bad |= !isfinite(v[i]);
-        tk.insert(v[i], e, k);
-        if (lrow) lrow[e] = v[i];
-      }
+  for (int i = 0; i < kCols; ++i) {
+    const int e = c0 + i;
+    if (e < E) {
+      bad |= !isfinite(v[i]);
+      tk.insert(v[i], e, k);
+      if (lrow) lrow[e] = v[i];
     }
   }
-  const float m = tk.v[0];
-
-  // pass 2: softmax denominator over all E experts, ascending e
-  float s = 0.f;
-  for (int c = 0; c < nchunks; ++c) {
-    float v[32];
-    src.load(c, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (32 * c + i < E) s += expf(v[i] - m);
-  }
-  const float inv_s = 1.0f / s;
-
-  // pass 3: per-expert sums of p over the tile's valid tokens (fixed
-  // butterfly within the warp, fixed warp order below)
-  for (int c = 0; c < nchunks; ++c) {
-    float v[32];
-    src.load(c, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = 32 * c + i;
-      if (e < E) {
-        float pe = valid ? expf(v[i] - m) * inv_s : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
-        if (lane == 0) red[warp * E_stride + e] = pe;
-      }
-    }
-  }
-
-  // renormalised top-k weights: p_j / sum_j' p_j' = ex_j / sum ex_j'
-  float ex[KMAX];
-  float den = 0.f;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    ex[j] = (j < k && tk.i[j] >= 0) ? expf(tk.v[j] - m) : 0.f;
-    den += ex[j];
+    es.cand_v[r][part][j] = tk.v[j];
+    es.cand_i[r][part][j] = tk.i[j];
+  }
+  __syncthreads();
+  if (part == 0) {
+    for (int pp = 1; pp < NPART; ++pp)
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) tk.insert(es.cand_v[r][pp][j], es.cand_i[r][pp][j], k);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      es.cand_v[r][0][j] = tk.v[j];
+      es.cand_i[r][0][j] = tk.i[j];
+    }
+    es.rowmax[r] = tk.v[0];
+  }
+  __syncthreads();
+  const float m = es.rowmax[r];
+  float s_loc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCols; ++i)
+    if (c0 + i < E) s_loc += expf(v[i] - m);
+  es.psum[r][part] = s_loc;
+  __syncthreads();
+
+  int eid[KMAX];
+  float ex[KMAX];
+  float den = 0.f;
+  if (part == 0) {
+    float s = es.psum[r][0];
+#pragma unroll
+    for (int pp = 1; pp < NPART; ++pp) s += es.psum[r][pp];
+    es.rowsum[r] = s;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      eid[j] = (j < k) ? tk.i[j] : -1;
+      ex[j] = (j < k && tk.i[j] >= 0) ? expf(tk.v[j] - m) : 0.f;
+      den += ex[j];
+      if (valid && eid[j] >= 0) atomicOr(&masks[q * E_stride + eid[j]], 1u << lane);
+    }
+  }
+  __syncthreads();
+
+  // per-expert probability sums over the tile's tokens
+  const float inv_s = 1.0f / es.rowsum[r];
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) {
+    const int e = c0 + i;
+    if (e < E) {
+      float pe = valid ? expf(v[i] - m) * inv_s : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+      if (lane == 0) red[q * E_stride + e] = pe;
+    }
   }
 
-  int rank[KMAX];
-  tile_ranks(masks, E_stride, E, k, tk.i, valid, rank, a.tile_cnt, a.n_tiles, tile);
-
-  if (valid) {
+  if (part == 0 && valid) {
+    const uint32_t below = (1u << lane) - 1u;
     const size_t base = static_cast<size_t>(t) * k;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
-        a.topk_idx[base + j] = tk.i[j];
+        int rk = 0;
+        if (eid[j] >= 0) {
+          rk = __popc(masks[q * E_stride + eid[j]] & below);
+          for (int w = 0; w < q; ++w) rk += __popc(masks[w * E_stride + eid[j]]);
+        }
+        a.topk_idx[base + j] = eid[j];
         a.topk_w[base + j] = ex[j] / den;
-        a.rank8[base + j] = static_cast<uint8_t>(rank[j]);
+        a.rank8[base + j] = static_cast<uint8_t>(rk);
       }
     }
-    if (bad) atomicOr(a.dev_status, MOE_DEV_NONFINITE);
+  }
+  if (bad && valid) atomicOr(a.dev_status, MOE_DEV_NONFINITE);
+  for (int x = tid; x < E; x += kTileTokens * NPART) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kTileTokens / 32; ++w) c += __popc(masks[w * E_stride + x]);
+    a.tile_cnt[static_cast<size_t>(x) * a.n_tiles + tile] = c;
   }
   __syncthreads();
-  for (int x = tid; x < E; x += kTileTokens) {
+  for (int x = tid; x < E; x += kTileTokens * NPART) {
     float sum = red[x];
 #pragma unroll
     for (int w = 1; w < kTileTokens / 32; ++w) sum += red[w * E_stride + x];
@@ -223,8 +274,9 @@ __global__ void gate_transpose_kernel(const uint16_t* __restrict__ gate,
   }
 }
 
-// Shared-memory carve-up of the router kernel (after the 1024-aligned
-// pipeline stages).
+// Shared-memory carve-up of the router kernel after the 1024-aligned
+// pipeline stages (the stages are reused as epilogue scratch once the
+// accumulator is complete).
 struct RouteSmem {
   uint64_t* full;
   uint64_t* empty;
@@ -249,8 +301,10 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
   return s;
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kTileTokens)
+// Two CTAs per SM (one's epilogue overlaps the other's loads) up to 512
+// threads; 1024-thread tiles (E > 128) run one per SM.
+template <int KMAX, int NPART>
+__global__ void __launch_bounds__(kTileTokens * NPART, NPART <= 4 ? 2 : 1)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_gate,
                       const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
@@ -259,12 +313,12 @@ __global__ void __launch_bounds__(kTileTokens)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
   const int S = a.stages;
-  const int E32 = (a.E_pad + 31) & ~31;
+  const int E32 = kCols * NPART;  // columns the epilogue reads (>= E_pad)
   const uint32_t a_bytes = kTileTokens * kBlockK * 2;
   const uint32_t b_bytes = static_cast<uint32_t>(a.E_pad) * kBlockK * 2;
   const uint32_t stage_bytes = a_bytes + b_bytes;
   RouteSmem sm = carve_route_smem(smem + static_cast<size_t>(S) * stage_bytes, S, E32);
-  const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(a.E_pad));
+  const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(E32));
 
   if (tile == 0 && tid == 0) *a.ticket = 0u;
   if (warp == 0) {
@@ -284,9 +338,9 @@ __global__ void __launch_bounds__(kTileTokens)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_gate);
   }
-  for (int i = tid; i < E32; i += kTileTokens)
+  for (int i = tid; i < E32; i += blockDim.x)
     sm.bias_s[i] = (a.bias != nullptr && i < a.E) ? a.bias[i] : 0.f;
-  for (int i = tid; i < 4 * E32; i += kTileTokens) sm.masks[i] = 0u;
+  for (int i = tid; i < 4 * E32; i += blockDim.x) sm.masks[i] = 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,8 +351,7 @@ __global__ void __launch_bounds__(kTileTokens)
   if (warp == 0 && lane == 0) {
     // TMA producer. The swizzled loads read 128-byte pieces of rows that lie
     // H*2 bytes apart; ahead of them, L2 prefetches through a plain (no
-    // swizzle) map fetch 512 contiguous bytes of each of the tile's rows, so
-    // DRAM sees whole row segments instead of scattered 128-byte pieces.
+    // swizzle) map fetch 512 contiguous bytes of each of the tile's rows.
     const int n_groups = (nk + kRowGroup - 1) / kRowGroup;
     for (int g = 0; g < kRouteGroupsAhead && g < n_groups; ++g)
       tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
@@ -348,8 +401,9 @@ __global__ void __launch_bounds__(kTileTokens)
   const int go = __syncthreads_and(done_ok && *sm.abort_flag == 0u);
   tc_fence_after();
   if (go) {
-    TmemSource src{tmem + (static_cast<uint32_t>(32 * warp) << 16), sm.bias_s};
-    route_epilogue<KMAX>(src, a, tile, sm.masks, sm.red, E32);
+    TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s};
+    auto& es = *reinterpret_cast<EpiSmem<KMAX, NPART>*>(smem);  // stages are free now
+    route_epilogue<KMAX, NPART>(src, a, tile, es, sm.masks, sm.red, E32);
   } else if (tid == 0) {
     atomicOr(a.dev_status, MOE_DEV_TIMEOUT);
   }
@@ -358,20 +412,21 @@ __global__ void __launch_bounds__(kTileTokens)
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kTileTokens) route_logits_kernel(RouteArgs a) {
+template <int KMAX, int NPART>
+__global__ void __launch_bounds__(kTileTokens * NPART) route_logits_kernel(RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
-  const int E32 = (a.E + 31) & ~31;
-  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw);
+  const int E32 = kCols * NPART;
+  auto& es = *reinterpret_cast<EpiSmem<KMAX, NPART>*>(smem_raw);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw + sizeof(EpiSmem<KMAX, NPART>));
   float* red = reinterpret_cast<float*>(masks + 4 * E32);
   if (tile == 0 && tid == 0) *a.ticket = 0u;
-  for (int i = tid; i < 4 * E32; i += kTileTokens) masks[i] = 0u;
+  for (int i = tid; i < 4 * E32; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
-  const int t = tile * kTileTokens + tid;
+  const int t = tile * kTileTokens + 32 * (warp & 3) + lane;
   GlobalSource src{a.logits_in + static_cast<size_t>(t < a.T ? t : 0) * a.E, a.E, t < a.T};
-  route_epilogue<KMAX>(src, a, tile, masks, red, E32);
+  route_epilogue<KMAX, NPART>(src, a, tile, es, masks, red, E32);
 }
 
 // Tile counts and ranks from caller-given indices. A slot is unusable if its
@@ -420,6 +475,11 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 
 // ------------------------------------------------------------------ host ----
 
+int route_parts(int E) {
+  const int p = (E + kCols - 1) / kCols;
+  return p <= 1 ? 1 : (p <= 2 ? 2 : (p <= 4 ? 4 : 8));
+}
+
 int route_stages(int E_pad) {
   // as many stages as fit in ~108 KB, so that two CTAs share an SM
   const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
@@ -428,7 +488,7 @@ int route_stages(int E_pad) {
 }
 
 size_t route_smem_bytes(int E_pad, int stages) {
-  const int E32 = (E_pad + 31) & ~31;
+  const int E32 = kCols * route_parts(E_pad);
   const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(E_pad) * kBlockK * 2;
   return 1024 + stage * stages + 8 * (2 * stages + 1) + 16 + 4 * E32 + 2 * 4 * 4 * E32;
 }
@@ -442,16 +502,32 @@ cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, 
   return cudaGetLastError();
 }
 
-template <int KMAX>
-cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                                const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+template <int KMAX, int NPART>
+cudaError_t launch_route_gemm_kp(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                                 const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+  // the epilogue scratch lives in the pipeline stages once they are free
+  const size_t stage_area = static_cast<size_t>(a.stages) *
+                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(a.E_pad) * kBlockK * 2);
+  if (sizeof(EpiSmem<KMAX, NPART>) > stage_area) return cudaErrorInvalidConfiguration;
   const size_t smem = route_smem_bytes(a.E_pad, a.stages);
-  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX>,
+  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX, NPART>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens, smem, st>>>(tm_x, tm_gate, tm_x_rows, a);
+  route_gemm_kernel<KMAX, NPART><<<a.n_tiles, kTileTokens * NPART, smem, st>>>(tm_x, tm_gate,
+                                                                               tm_x_rows, a);
   return cudaGetLastError();
+}
+
+template <int KMAX>
+cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                                const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+  switch (route_parts(a.E)) {
+    case 1: return launch_route_gemm_kp<KMAX, 1>(tm_x, tm_gate, tm_x_rows, a, st);
+    case 2: return launch_route_gemm_kp<KMAX, 2>(tm_x, tm_gate, tm_x_rows, a, st);
+    case 4: return launch_route_gemm_kp<KMAX, 4>(tm_x, tm_gate, tm_x_rows, a, st);
+    default: return launch_route_gemm_kp<KMAX, 8>(tm_x, tm_gate, tm_x_rows, a, st);
+  }
 }
 
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
@@ -461,16 +537,31 @@ cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gat
   return launch_route_gemm_k<8>(tm_x, tm_gate, tm_x_rows, a, st);
 }
 
-cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
-  const int E32 = (a.E + 31) & ~31;
-  const size_t smem = 2 * 4 * 4 * static_cast<size_t>(E32);
-  if (a.k <= 2)
-    route_logits_kernel<2><<<a.n_tiles, kTileTokens, smem, st>>>(a);
-  else if (a.k <= 4)
-    route_logits_kernel<4><<<a.n_tiles, kTileTokens, smem, st>>>(a);
-  else
-    route_logits_kernel<8><<<a.n_tiles, kTileTokens, smem, st>>>(a);
+template <int KMAX, int NPART>
+cudaError_t launch_route_logits_kp(const RouteArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(EpiSmem<KMAX, NPART>) + 2 * 4 * 4 * kCols * NPART;
+  cudaError_t err = cudaFuncSetAttribute(route_logits_kernel<KMAX, NPART>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  route_logits_kernel<KMAX, NPART><<<a.n_tiles, kTileTokens * NPART, smem, st>>>(a);
   return cudaGetLastError();
+}
+
+template <int KMAX>
+cudaError_t launch_route_logits_k(const RouteArgs& a, cudaStream_t st) {
+  switch (route_parts(a.E)) {
+    case 1: return launch_route_logits_kp<KMAX, 1>(a, st);
+    case 2: return launch_route_logits_kp<KMAX, 2>(a, st);
+    case 4: return launch_route_logits_kp<KMAX, 4>(a, st);
+    default: return launch_route_logits_kp<KMAX, 8>(a, st);
+  }
+}
+
+cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
+  if (a.k <= 2) return launch_route_logits_k<2>(a, st);
+  if (a.k <= 4) return launch_route_logits_k<4>(a, st);
+  return launch_route_logits_k<8>(a, st);
 }
 
 cudaError_t launch_rank(const RankArgs& a, cudaStream_t st) {
