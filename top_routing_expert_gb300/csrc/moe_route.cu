@@ -91,51 +91,76 @@ __device__ __forceinline__ void tile_ranks(uint32_t* masks, int E_stride, int E,
 
 // --------------------------------------------------------------- sources ----
 
-// Each epilogue thread owns one token row (TMEM lane) and one part of 32
-// expert columns of it: a CTA runs kTileTokens * NPART threads, warp w
-// reading lane quadrant w % 4 and part w / 4.
-constexpr int kCols = 32;
+// Each epilogue thread owns one token row (TMEM lane) and one part of `cpt`
+// expert columns of it: a CTA runs kTileTokens * npart threads, warp w
+// reading lane quadrant w % 4 and part w / 4. Columns are handled 8 at a
+// time in loops that are not unrolled, which keeps the code small.
+constexpr int kChunk = 8;
 
-// Logits of the thread's row and part from TMEM (GEMM path), plus the bias.
+// Logits of the thread's row from TMEM (GEMM path), plus the bias.
 struct TmemSource {
   uint32_t taddr;       // TMEM address of (this warp's lane quadrant, column 0)
   const float* bias_s;  // shared, zero past E
-  __device__ __forceinline__ void load(int part, float (&v)[kCols]) const {
-    uint32_t r[kCols];
-    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(kCols * part), r);
+  __device__ __forceinline__ void load(int c, float (&v)[kChunk]) const {
+    uint32_t r[kChunk];
+    tmem_ld_32x32b_x8(taddr + static_cast<uint32_t>(c), r);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < kCols; ++i) v[i] = __uint_as_float(r[i]) + bias_s[kCols * part + i];
+    for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]) + bias_s[c + i];
   }
 };
 
-// Logits of the thread's row and part from global memory (logits entry point).
+// Logits of the thread's row from global memory (logits entry point).
 struct GlobalSource {
   const float* row;
   int E;
   bool valid;
-  __device__ __forceinline__ void load(int part, float (&v)[kCols]) const {
+  __device__ __forceinline__ void load(int c, float (&v)[kChunk]) const {
 #pragma unroll
-    for (int i = 0; i < kCols; ++i) {
-      const int e = kCols * part + i;
+    for (int i = 0; i < kChunk; ++i) {
+      const int e = c + i;
       v[i] = (valid && e < E) ? row[e] : 0.f;
     }
   }
 };
 
-// Shared scratch of the routing epilogue.
-template <int KMAX, int NPART>
-struct EpiSmem {
-  float cand_v[kTileTokens][NPART][KMAX];  // per-part top-k lists; part 0 ends merged
-  int cand_i[kTileTokens][NPART][KMAX];
-  float psum[kTileTokens][NPART];          // per-part softmax partial sums
-  float rowmax[kTileTokens];
-  float rowsum[kTileTokens];
+// Parts per token row (epilogue warps per TMEM lane quadrant) and columns
+// per part: a multiple of 8, npart * cpt >= E.
+__host__ __device__ inline int route_parts_of(int E) {
+  return E <= 16 ? 1 : (E <= 32 ? 2 : (E <= 128 ? 4 : 8));
+}
+__host__ __device__ inline int route_cpt_of(int E) {
+  const int n = route_parts_of(E);
+  return ((E + n - 1) / n + kChunk - 1) / kChunk * kChunk;
+}
+
+// Shared scratch of the routing epilogue, laid out for `npart` parts.
+struct EpiScratch {
+  float* cand_v;  // [kTileTokens][npart][KMAX] per-part top-k; part 0 ends merged
+  int* cand_i;
+  float* psum;    // [kTileTokens][npart] per-part softmax partial sums
+  float* rowmax;  // [kTileTokens]
+  float* rowsum;  // [kTileTokens]
 };
+
+__host__ __device__ inline size_t epi_scratch_bytes(int npart, int kmax) {
+  return static_cast<size_t>(kTileTokens) * npart * kmax * 8 + static_cast<size_t>(kTileTokens) * npart * 4 +
+         2 * kTileTokens * 4;
+}
+
+__device__ __forceinline__ EpiScratch carve_epi(uint8_t* p, int npart, int kmax) {
+  EpiScratch e;
+  e.cand_v = reinterpret_cast<float*>(p);
+  e.cand_i = reinterpret_cast<int*>(e.cand_v + kTileTokens * npart * kmax);
+  e.psum = reinterpret_cast<float*>(e.cand_i + kTileTokens * npart * kmax);
+  e.rowmax = e.psum + kTileTokens * npart;
+  e.rowsum = e.rowmax + kTileTokens;
+  return e;
+}
 
 // The routing epilogue shared by both paths; identical arithmetic, so equal
 // logits give bit-identical results. All threads of the CTA call it.
-//   1. each thread: top-k of its 32 columns (ascending expert order);
+//   1. each thread: top-k of its columns (ascending expert order);
 //   2. part 0 merges the parts' lists in part order -> the token's top-k and
 //      its max m (the order-defined comparator makes the merge exact);
 //   3. softmax denominator: per-part sums of exp(l - m), added in part order;
@@ -143,67 +168,75 @@ struct EpiSmem {
 //   5. in-tile arrival ranks and per-tile expert counts from warp bit masks;
 //   6. per-expert sums of p over the tile's tokens (fixed butterfly per warp,
 //      then quadrants in order).
-template <int KMAX, int NPART, class Src>
+template <int KMAX, class Src>
 __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
-                                               EpiSmem<KMAX, NPART>& es, uint32_t* masks,
-                                               float* red, int E_stride) {
+                                               EpiScratch es, uint32_t* masks, float* red,
+                                               int E_stride, int npart, int cpt) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = warp & 3, part = warp >> 2;
   const int r = 32 * q + lane;
   const int E = a.E, k = a.k;
   const int t = tile * kTileTokens + r;
   const bool valid = t < a.T;
-  const int c0 = kCols * part;
+  const int c0 = cpt * part;
+  const int cend = c0 + cpt;
 
-  float v[kCols];
-  src.load(part, v);
   TopK<KMAX> tk;
   tk.init();
   bool bad = false;
   float* lrow = (a.logits_out && valid) ? a.logits_out + static_cast<size_t>(t) * E : nullptr;
+#pragma unroll 1
+  for (int c = c0; c < cend; c += kChunk) {
+    float v[kChunk];
+    src.load(c, v);
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) {
-    const int e = c0 + i;
-    if (e < E) {
-      bad |= !isfinite(v[i]);
-      tk.insert(v[i], e, k);
-      if (lrow) lrow[e] = v[i];
+    for (int i = 0; i < kChunk; ++i) {
+      const int e = c + i;
+      if (e < E) {
+        bad |= !isfinite(v[i]);
+        tk.insert(v[i], e, k);
+        if (lrow) lrow[e] = v[i];
+      }
     }
   }
+  const int cbase = (r * npart + part) * KMAX;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    es.cand_v[r][part][j] = tk.v[j];
-    es.cand_i[r][part][j] = tk.i[j];
+    es.cand_v[cbase + j] = tk.v[j];
+    es.cand_i[cbase + j] = tk.i[j];
   }
   __syncthreads();
   if (part == 0) {
-    for (int pp = 1; pp < NPART; ++pp)
+#pragma unroll 1
+    for (int pp = 1; pp < npart; ++pp) {
+      const int b = (r * npart + pp) * KMAX;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) tk.insert(es.cand_v[r][pp][j], es.cand_i[r][pp][j], k);
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      es.cand_v[r][0][j] = tk.v[j];
-      es.cand_i[r][0][j] = tk.i[j];
+        if (j < k) tk.insert(es.cand_v[b + j], es.cand_i[b + j], k);
     }
     es.rowmax[r] = tk.v[0];
   }
   __syncthreads();
   const float m = es.rowmax[r];
   float s_loc = 0.f;
+#pragma unroll 1
+  for (int c = c0; c < cend; c += kChunk) {
+    float v[kChunk];
+    src.load(c, v);
 #pragma unroll
-  for (int i = 0; i < kCols; ++i)
-    if (c0 + i < E) s_loc += expf(v[i] - m);
-  es.psum[r][part] = s_loc;
+    for (int i = 0; i < kChunk; ++i)
+      if (c + i < E) s_loc += expf(v[i] - m);
+  }
+  es.psum[r * npart + part] = s_loc;
   __syncthreads();
 
   int eid[KMAX];
   float ex[KMAX];
   float den = 0.f;
   if (part == 0) {
-    float s = es.psum[r][0];
-#pragma unroll
-    for (int pp = 1; pp < NPART; ++pp) s += es.psum[r][pp];
+    float s = es.psum[r * npart];
+#pragma unroll 1
+    for (int pp = 1; pp < npart; ++pp) s += es.psum[r * npart + pp];
     es.rowsum[r] = s;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
@@ -217,14 +250,19 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
 
   // per-expert probability sums over the tile's tokens
   const float inv_s = 1.0f / es.rowsum[r];
+#pragma unroll 1
+  for (int c = c0; c < cend; c += kChunk) {
+    float v[kChunk];
+    src.load(c, v);
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) {
-    const int e = c0 + i;
-    if (e < E) {
-      float pe = valid ? expf(v[i] - m) * inv_s : 0.f;
+    for (int i = 0; i < kChunk; ++i) {
+      const int e = c + i;
+      if (e < E) {
+        float pe = valid ? expf(v[i] - m) * inv_s : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
-      if (lane == 0) red[q * E_stride + e] = pe;
+        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+        if (lane == 0) red[q * E_stride + e] = pe;
+      }
     }
   }
 
@@ -246,14 +284,14 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
     }
   }
   if (bad && valid) atomicOr(a.dev_status, MOE_DEV_NONFINITE);
-  for (int x = tid; x < E; x += kTileTokens * NPART) {
+  for (int x = tid; x < E; x += blockDim.x) {
     int c = 0;
 #pragma unroll
     for (int w = 0; w < kTileTokens / 32; ++w) c += __popc(masks[w * E_stride + x]);
     a.tile_cnt[static_cast<size_t>(x) * a.n_tiles + tile] = c;
   }
   __syncthreads();
-  for (int x = tid; x < E; x += kTileTokens * NPART) {
+  for (int x = tid; x < E; x += blockDim.x) {
     float sum = red[x];
 #pragma unroll
     for (int w = 1; w < kTileTokens / 32; ++w) sum += red[w * E_stride + x];
@@ -301,10 +339,10 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
   return s;
 }
 
-// Two CTAs per SM (one's epilogue overlaps the other's loads) up to 512
-// threads; 1024-thread tiles (E > 128) run one per SM.
-template <int KMAX, int NPART>
-__global__ void __launch_bounds__(kTileTokens * NPART, NPART <= 4 ? 2 : 1)
+// Up to 512 threads two CTAs share an SM (one's epilogue overlaps the
+// other's loads); the register budget allows that at 64 per thread.
+template <int KMAX>
+__global__ void __launch_bounds__(kTileTokens * 8, 1)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_gate,
                       const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
@@ -313,7 +351,9 @@ __global__ void __launch_bounds__(kTileTokens * NPART, NPART <= 4 ? 2 : 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
   const int S = a.stages;
-  const int E32 = kCols * NPART;  // columns the epilogue reads (>= E_pad)
+  const int npart = route_parts_of(a.E), cpt = route_cpt_of(a.E);
+  const int ecols = npart * cpt;                // columns the epilogue reads (>= E)
+  const int E32 = ((ecols > a.E_pad ? ecols : a.E_pad) + 31) & ~31;
   const uint32_t a_bytes = kTileTokens * kBlockK * 2;
   const uint32_t b_bytes = static_cast<uint32_t>(a.E_pad) * kBlockK * 2;
   const uint32_t stage_bytes = a_bytes + b_bytes;
@@ -402,8 +442,9 @@ __global__ void __launch_bounds__(kTileTokens * NPART, NPART <= 4 ? 2 : 1)
   tc_fence_after();
   if (go) {
     TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s};
-    auto& es = *reinterpret_cast<EpiSmem<KMAX, NPART>*>(smem);  // stages are free now
-    route_epilogue<KMAX, NPART>(src, a, tile, es, sm.masks, sm.red, E32);
+    // the pipeline stages are free now: they hold the epilogue scratch
+    route_epilogue<KMAX>(src, a, tile, carve_epi(smem, npart, KMAX), sm.masks, sm.red, E32,
+                         npart, cpt);
   } else if (tid == 0) {
     atomicOr(a.dev_status, MOE_DEV_TIMEOUT);
   }
@@ -412,21 +453,22 @@ __global__ void __launch_bounds__(kTileTokens * NPART, NPART <= 4 ? 2 : 1)
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
-template <int KMAX, int NPART>
-__global__ void __launch_bounds__(kTileTokens * NPART) route_logits_kernel(RouteArgs a) {
+template <int KMAX>
+__global__ void __launch_bounds__(kTileTokens * 8, 1) route_logits_kernel(RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
-  const int E32 = kCols * NPART;
-  auto& es = *reinterpret_cast<EpiSmem<KMAX, NPART>*>(smem_raw);
-  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw + sizeof(EpiSmem<KMAX, NPART>));
+  const int npart = route_parts_of(a.E), cpt = route_cpt_of(a.E);
+  const int E32 = (npart * cpt + 31) & ~31;
+  EpiScratch es = carve_epi(smem_raw, npart, KMAX);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw + epi_scratch_bytes(npart, KMAX));
   float* red = reinterpret_cast<float*>(masks + 4 * E32);
   if (tile == 0 && tid == 0) *a.ticket = 0u;
   for (int i = tid; i < 4 * E32; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
   const int t = tile * kTileTokens + 32 * (warp & 3) + lane;
   GlobalSource src{a.logits_in + static_cast<size_t>(t < a.T ? t : 0) * a.E, a.E, t < a.T};
-  route_epilogue<KMAX, NPART>(src, a, tile, es, masks, red, E32);
+  route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, npart, cpt);
 }
 
 // Tile counts and ranks from caller-given indices. A slot is unusable if its
@@ -475,11 +517,6 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 
 // ------------------------------------------------------------------ host ----
 
-int route_parts(int E) {
-  const int p = (E + kCols - 1) / kCols;
-  return p <= 1 ? 1 : (p <= 2 ? 2 : (p <= 4 ? 4 : 8));
-}
-
 int route_stages(int E_pad) {
   // as many stages as fit in ~108 KB, so that two CTAs share an SM
   const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
@@ -488,7 +525,9 @@ int route_stages(int E_pad) {
 }
 
 size_t route_smem_bytes(int E_pad, int stages) {
-  const int E32 = kCols * route_parts(E_pad);
+  const int E = E_pad;  // upper bound for the epilogue's column span
+  const int ecols = route_parts_of(E) * route_cpt_of(E);
+  const int E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
   const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(E_pad) * kBlockK * 2;
   return 1024 + stage * stages + 8 * (2 * stages + 1) + 16 + 4 * E32 + 2 * 4 * 4 * E32;
 }
@@ -502,65 +541,48 @@ cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, 
   return cudaGetLastError();
 }
 
-template <int KMAX, int NPART>
-cudaError_t launch_route_gemm_kp(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                                 const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
-  // the epilogue scratch lives in the pipeline stages once they are free
-  const size_t stage_area = static_cast<size_t>(a.stages) *
-                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(a.E_pad) * kBlockK * 2);
-  if (sizeof(EpiSmem<KMAX, NPART>) > stage_area) return cudaErrorInvalidConfiguration;
-  const size_t smem = route_smem_bytes(a.E_pad, a.stages);
-  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX, NPART>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  route_gemm_kernel<KMAX, NPART><<<a.n_tiles, kTileTokens * NPART, smem, st>>>(tm_x, tm_gate,
-                                                                               tm_x_rows, a);
-  return cudaGetLastError();
-}
-
 template <int KMAX>
 cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
                                 const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
-  switch (route_parts(a.E)) {
-    case 1: return launch_route_gemm_kp<KMAX, 1>(tm_x, tm_gate, tm_x_rows, a, st);
-    case 2: return launch_route_gemm_kp<KMAX, 2>(tm_x, tm_gate, tm_x_rows, a, st);
-    case 4: return launch_route_gemm_kp<KMAX, 4>(tm_x, tm_gate, tm_x_rows, a, st);
-    default: return launch_route_gemm_kp<KMAX, 8>(tm_x, tm_gate, tm_x_rows, a, st);
-  }
+  const int npart = route_parts_of(a.E);
+  // the epilogue scratch lives in the pipeline stages once they are free
+  const size_t stage_area = static_cast<size_t>(a.stages) *
+                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(a.E_pad) * kBlockK * 2);
+  if (epi_scratch_bytes(npart, KMAX) > stage_area) return cudaErrorInvalidConfiguration;
+  const size_t smem = route_smem_bytes(a.E_pad, a.stages);
+  cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(tm_x, tm_gate, tm_x_rows, a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
                               const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
   if (a.k <= 2) return launch_route_gemm_k<2>(tm_x, tm_gate, tm_x_rows, a, st);
   if (a.k <= 4) return launch_route_gemm_k<4>(tm_x, tm_gate, tm_x_rows, a, st);
+  if (a.k <= 6) return launch_route_gemm_k<6>(tm_x, tm_gate, tm_x_rows, a, st);
   return launch_route_gemm_k<8>(tm_x, tm_gate, tm_x_rows, a, st);
-}
-
-template <int KMAX, int NPART>
-cudaError_t launch_route_logits_kp(const RouteArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(EpiSmem<KMAX, NPART>) + 2 * 4 * 4 * kCols * NPART;
-  cudaError_t err = cudaFuncSetAttribute(route_logits_kernel<KMAX, NPART>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  route_logits_kernel<KMAX, NPART><<<a.n_tiles, kTileTokens * NPART, smem, st>>>(a);
-  return cudaGetLastError();
 }
 
 template <int KMAX>
 cudaError_t launch_route_logits_k(const RouteArgs& a, cudaStream_t st) {
-  switch (route_parts(a.E)) {
-    case 1: return launch_route_logits_kp<KMAX, 1>(a, st);
-    case 2: return launch_route_logits_kp<KMAX, 2>(a, st);
-    case 4: return launch_route_logits_kp<KMAX, 4>(a, st);
-    default: return launch_route_logits_kp<KMAX, 8>(a, st);
-  }
+  const int npart = route_parts_of(a.E);
+  const int E32 = (npart * route_cpt_of(a.E) + 31) & ~31;
+  const size_t smem = epi_scratch_bytes(npart, KMAX) + 2 * 4 * 4 * static_cast<size_t>(E32);
+  cudaError_t err = cudaFuncSetAttribute(route_logits_kernel<KMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  route_logits_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
   if (a.k <= 2) return launch_route_logits_k<2>(a, st);
   if (a.k <= 4) return launch_route_logits_k<4>(a, st);
+  if (a.k <= 6) return launch_route_logits_k<6>(a, st);
   return launch_route_logits_k<8>(a, st);
 }
 

@@ -70,6 +70,10 @@ WORKLOADS = {
 PROFILE_WORKLOADS = {
     "ffn_profile": Workload("ffn_profile", 4096, 4096, 2, 2, 14336, 1.25,
                             note="profiler capture case of the large-expert FFN"),
+    # the large-expert router and dispatch (T=32768, H=4096, E=8, k=2) with a
+    # 64-wide FFN: about 1.5 GB on the device
+    "route_profile": Workload("route_profile", 32768, 4096, 8, 2, 64, 1.25,
+                              note="profiler capture case of the large-expert router"),
 }
 # Positional aliases, in the order the workloads are usually listed.
 WORKLOAD_ORDER = ["tiny", "imbalanced", "large_expert", "fine_grained", "many_expert"]
