@@ -203,31 +203,30 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
-    """End to end through the public API with host buffers: copy x in, read
-    y and aux out, every step, inside the timed region."""
+    """End to end through the public API with host buffers: every step is one
+    micro-batch of moe_layer_fwd_host - its tokens copied in from pinned host
+    memory, the layer, its output and aux copied back to the host - with the
+    copies of neighbouring micro-batches overlapping the layer on three
+    streams. Timed from before the first copy-in to after the last copy-out."""
     T, H = inp["x"].shape
+    pipe = moe.HostPipeline(s, device=dev)
     x_host = inp["x"].pin_memory()
     y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    aux_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(d["x"])
+    aux_host = torch.empty(max(args.steps, args.warmup), dtype=torch.float32).pin_memory()
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_fwd(s, x_dev, d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux, ws=ws,
-                          stream=stream)
-        y_host.copy_(y, non_blocking=True)
-        aux_host.copy_(aux, non_blocking=True)
+    def run(n):
+        return pipe.run([x_host] * n, [y_host] * n, d["gate"], d["bias"], d["W1"], d["W2"],
+                        aux_host)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    run(args.warmup).synchronize()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e0.record(pipe.streams[1])
+    out = run(args.steps)
+    e1.record(out)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
@@ -357,7 +356,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=W.WORKLOAD_ORDER + list(W.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

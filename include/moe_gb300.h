@@ -173,6 +173,37 @@ moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* 
                          int32_t* offsets, int32_t* dest_row, uint32_t* dev_status,
                          void* ws, size_t ws_bytes, void* stream, void* const* events);
 
+/* Bytes of device workspace moe_layer_fwd_host needs for micro-batches of
+ * this shape: the layer workspace plus two token and two output buffers.
+ * Host only. */
+moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes);
+
+/* Host-to-host layer forward over n_micro micro-batches of s->T tokens each,
+ * pipelined over three caller streams - the dual-stream, micro-batch overlap
+ * of the MoE comm bottleneck page, section 5.2, with the host<->device copies
+ * in the role of the dispatch/combine traffic: while micro-batch i runs the
+ * layer on streams[0], micro-batch i+1's tokens are copied in on streams[1]
+ * and micro-batch i-1's outputs are copied out on streams[2].
+ *   x_host[i], y_host[i] (i < n_micro): HOST pointers to [T,H] bf16 tokens
+ *        and outputs; page-locked memory (cudaHostAlloc / cudaHostRegister)
+ *        is needed for the copies to overlap. The same pointer may repeat.
+ *   aux_host: HOST array of n_micro floats, or NULL.
+ *   gate, gate_bias (nullable), W1, W2: device, as in moe_layer_fwd.
+ *   dev_status: device word or NULL.
+ *   ws: device, >= moe_host_workspace_size bytes.
+ *   streams: host array of 3 cudaStream_t (compute, copy-in, copy-out),
+ *        owned by the caller; they must be distinct streams (not the legacy
+ *        default stream, which would serialise them).
+ *   events: host array of 6 cudaEvent_t created by the caller (timing may be
+ *        disabled); they order the buffers between the streams.
+ * Everything is enqueued and the call returns; y_host and aux_host are valid
+ * once streams[2] has completed. */
+moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
+                              moe_bf16* const* y_host, float* aux_host, const moe_bf16* gate,
+                              const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                              uint32_t* dev_status, void* ws, size_t ws_bytes,
+                              void* const* streams, void* const* events);
+
 /* moe_permute for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it serves code that may not call
  * cudaMalloc or hold a workspace: a plugin inside a runtime that owns all

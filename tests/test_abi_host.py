@@ -116,6 +116,29 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert lib.moe_combine(None, f, f, f, f, None) == 1
 
 
+def test_host_pipeline_entry_rejects_bad_arguments(lib):
+    s = _shape()
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    n = ctypes.c_size_t()
+    assert lib.moe_host_workspace_size(ctypes.byref(s), ctypes.byref(n)) == 0
+    assert n.value > _status(lib, s)[1]          # layer workspace + I/O buffers
+    ptrs = (P * 1)(f)
+    # NULL streams / events / host pointer lists
+    assert lib.moe_layer_fwd_host(ctypes.byref(s), 1, ptrs, ptrs, None, f, None, f, f, None, f,
+                                  n.value, None, ptrs) == 1
+    assert lib.moe_layer_fwd_host(ctypes.byref(s), 1, None, ptrs, None, f, None, f, f, None, f,
+                                  n.value, ptrs, ptrs) == 1
+    # workspace too small, negative count, bad shape
+    assert lib.moe_layer_fwd_host(ctypes.byref(s), 1, ptrs, ptrs, None, f, None, f, f, None, f,
+                                  n.value - 1, ptrs, ptrs) == 4
+    assert lib.moe_layer_fwd_host(ctypes.byref(s), -1, ptrs, ptrs, None, f, None, f, f, None, f,
+                                  n.value, ptrs, ptrs) == 2
+    bad = _shape(H=96)
+    assert lib.moe_layer_fwd_host(ctypes.byref(bad), 1, ptrs, ptrs, None, f, None, f, f, None, f,
+                                  n.value, ptrs, ptrs) == 3
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert moe.status_str(code)

@@ -479,3 +479,32 @@ def test_layer_full_size_workloads_sampled(name):
     inp = W.make_inputs(w, seed=0)
     g = _layer_gpu(w, inp)
     _check_layer(w, inp, g, sample=W.sample_rows(w.T, 1024, seed=1).numpy())
+
+
+def test_layer_host_pipeline_equals_device_layer():
+    """moe_layer_fwd_host over three micro-batches (copies overlapped with
+    the layer on three streams) gives each micro-batch's moe_layer_fwd
+    output bit for bit."""
+    w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="pipe")
+    shape = _shape(w.T, w.H, w.E, w.k, w.h, w.cf)
+    base = W.make_inputs(w, seed=21)
+    xs = [W.make_inputs(w, seed=s, with_weights=False)["x"] for s in (22, 23, 24)]
+    dv = {n: base[n].to(DEV) for n in ("gate", "W1", "W2")}
+    bias = base["bias"].to(DEV)
+    pipe = moe.HostPipeline(shape)
+    x_host = [x.pin_memory() for x in xs]
+    y_host = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    aux_host = torch.zeros(len(xs), dtype=torch.float32).pin_memory()
+    status = _status()
+    out_stream = pipe.run(x_host, y_host, dv["gate"], bias, dv["W1"], dv["W2"], aux_host, status)
+    out_stream.synchronize()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ws = moe.Workspace(shape)
+    for i, x in enumerate(xs):
+        y = _zeros((w.T, w.H), torch.bfloat16)
+        aux = _zeros(1, torch.float32)
+        moe.moe_layer_fwd(shape, x.to(DEV), dv["gate"], bias, dv["W1"], dv["W2"], y, aux=aux, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), y_host[i]), i
+        assert float(aux.item()) == float(aux_host[i])

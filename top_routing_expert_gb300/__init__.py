@@ -20,7 +20,8 @@ from ._build import LIB, build  # noqa: F401  (re-exported)
 __all__ = [
     "MoeError", "MoeShape", "load_library", "capacity", "workspace_size", "status_str",
     "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
-    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
+    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
+    "host_workspace_size", "HostPipeline", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
 
@@ -28,7 +29,8 @@ DEV_BAD_INDEX, DEV_DUP_INDEX, DEV_NONFINITE, DEV_TIMEOUT = 1, 2, 4, 8
 LAYER_NUM_EVENTS = 7
 EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "moe_status_str",
                     "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
-                    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc"]
+                    "moe_combine", "moe_layer_fwd", "moe_permute_noalloc",
+                    "moe_host_workspace_size", "moe_layer_fwd_host"]
 
 
 class MoeError(RuntimeError):
@@ -82,6 +84,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_layer_fwd.argtypes = [S] + [_P] * 16 + [ctypes.c_size_t, _P, _P]
     lib.moe_permute_noalloc.restype = ctypes.c_int
     lib.moe_permute_noalloc.argtypes = [S] + [_P] * 9
+    lib.moe_host_workspace_size.restype = ctypes.c_int
+    lib.moe_host_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_layer_fwd_host.restype = ctypes.c_int
+    lib.moe_layer_fwd_host.argtypes = [S, ctypes.c_int64] + [_P] * 9 + [ctypes.c_size_t, _P, _P]
     _lib = lib
     return lib
 
@@ -252,3 +258,63 @@ def moe_permute_noalloc(shape, x, topk_idx, kept_counts, offsets, dest_row, src_
         _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
         _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(dev_status, torch.int32, "dev_status"),
         _stream(stream)))
+
+
+def host_workspace_size(shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_host_workspace_size",
+           load_library().moe_host_workspace_size(ctypes.byref(_shape(shape)), ctypes.byref(n)))
+    return n.value
+
+
+def _host_ptr(t: torch.Tensor, name: str) -> int:
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous() or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a contiguous bf16 host tensor")
+    return t.data_ptr()
+
+
+class HostPipeline:
+    """Owns what moe_layer_fwd_host needs besides the weights: the device
+    workspace, three CUDA streams (compute, copy-in, copy-out) and six
+    events. Host token/output tensors should be pinned for the copies to
+    overlap the layer."""
+
+    def __init__(self, shape, device="cuda"):
+        self.shape = _shape(shape)
+        self.nbytes = host_workspace_size(self.shape)
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
+        self.events = [torch.cuda.Event() for _ in range(6)]
+        for e in self.events:          # create the handles
+            e.record(self.streams[0])
+
+    def run(self, x_host, y_host, gate, gate_bias, W1, W2, aux_host=None, dev_status=None):
+        """Enqueues the layer over the micro-batches x_host[i] -> y_host[i]
+        (lists of [T,H] bf16 host tensors); returns the copy-out stream,
+        which the caller synchronises before reading y_host / aux_host."""
+        n = len(x_host)
+        if len(y_host) != n:
+            raise ValueError("x_host and y_host need the same length")
+        xs = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "x_host") for t in x_host])
+        ys = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "y_host") for t in y_host])
+        aux = None
+        if aux_host is not None:
+            if aux_host.is_cuda or aux_host.dtype != torch.float32 or aux_host.numel() < n:
+                raise ValueError("aux_host must be a float32 host tensor with >= n entries")
+            aux = aux_host.data_ptr()
+        st = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
+        ev = (ctypes.c_void_p * 6)(*[e.cuda_event for e in self.events])
+        _check("moe_layer_fwd_host", load_library().moe_layer_fwd_host(
+            ctypes.byref(self.shape), n, xs, ys, aux, _ptr(gate, torch.bfloat16, "gate"),
+            _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
+            _ptr(W2, torch.bfloat16, "W2"), _ptr(dev_status, torch.int32, "dev_status"),
+            self.buf.data_ptr(), self.nbytes, st, ev))
+        return self.streams[2]
+
+
+def moe_layer_fwd_host(pipeline: HostPipeline, x_host, y_host, gate, gate_bias, W1, W2,
+                       aux_host=None, dev_status=None):
+    """C-ABI name for HostPipeline.run."""
+    return pipeline.run(x_host, y_host, gate, gate_bias, W1, W2, aux_host, dev_status)

@@ -569,4 +569,83 @@ moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* 
   return MOE_OK;
 }
 
+moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_NULL;
+  MOE_TRY(check_shape(s));
+  const Dims d = dims_of(s);
+  const size_t io = (static_cast<size_t>(d.T) * d.H * 2 + 255) & ~size_t(255);
+  *bytes = layout(d, nullptr, nullptr) + 4 * io + 512;
+  return MOE_OK;
+}
+
+moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
+                              moe_bf16* const* y_host, float* aux_host, const moe_bf16* gate,
+                              const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                              uint32_t* dev_status, void* ws, size_t ws_bytes,
+                              void* const* streams, void* const* events) {
+  MOE_TRY(check_shape(s));
+  if (n_micro < 0) return MOE_ERR_SHAPE;
+  if (x_host == nullptr || y_host == nullptr || streams == nullptr || events == nullptr)
+    return MOE_ERR_NULL;
+  MOE_REQUIRE(gate);
+  MOE_REQUIRE(W1);
+  MOE_REQUIRE(W2);
+  MOE_OPTIONAL(gate_bias);
+  MOE_OPTIONAL(dev_status);
+  if (ws == nullptr) return MOE_ERR_NULL;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  size_t need = 0;
+  MOE_TRY(moe_host_workspace_size(s, &need));
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  for (int i = 0; i < 3; ++i)
+    if (streams[i] == nullptr) return MOE_ERR_NULL;
+  for (int i = 0; i < 6; ++i)
+    if (events[i] == nullptr) return MOE_ERR_NULL;
+  for (int64_t i = 0; i < n_micro; ++i)
+    if (x_host[i] == nullptr || y_host[i] == nullptr) return MOE_ERR_NULL;
+
+  const Dims d = dims_of(s);
+  const size_t layer_bytes = layout(d, nullptr, nullptr);
+  const size_t tok_bytes = static_cast<size_t>(d.T) * d.H * 2;
+  const size_t io = (tok_bytes + 255) & ~size_t(255);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  moe_bf16* xbuf[2] = {reinterpret_cast<moe_bf16*>(base + layer_bytes),
+                       reinterpret_cast<moe_bf16*>(base + layer_bytes + io)};
+  moe_bf16* ybuf[2] = {reinterpret_cast<moe_bf16*>(base + layer_bytes + 2 * io),
+                       reinterpret_cast<moe_bf16*>(base + layer_bytes + 3 * io)};
+  float* auxbuf[2] = {reinterpret_cast<float*>(base + layer_bytes + 4 * io),
+                      reinterpret_cast<float*>(base + layer_bytes + 4 * io + 256)};
+  cudaStream_t sc = static_cast<cudaStream_t>(streams[0]);
+  cudaStream_t sin = static_cast<cudaStream_t>(streams[1]);
+  cudaStream_t sout = static_cast<cudaStream_t>(streams[2]);
+  cudaEvent_t ev_in[2] = {static_cast<cudaEvent_t>(events[0]), static_cast<cudaEvent_t>(events[1])};
+  cudaEvent_t ev_layer[2] = {static_cast<cudaEvent_t>(events[2]),
+                             static_cast<cudaEvent_t>(events[3])};
+  cudaEvent_t ev_out[2] = {static_cast<cudaEvent_t>(events[4]), static_cast<cudaEvent_t>(events[5])};
+
+  for (int64_t i = 0; i < n_micro; ++i) {
+    const int b = static_cast<int>(i & 1);
+    // tokens in: buffer b is free once the layer of micro-batch i-2 is done
+    if (i >= 2) MOE_CUDA(cudaStreamWaitEvent(sin, ev_layer[b], 0));
+    if (tok_bytes)
+      MOE_CUDA(cudaMemcpyAsync(xbuf[b], x_host[i], tok_bytes, cudaMemcpyHostToDevice, sin));
+    MOE_CUDA(cudaEventRecord(ev_in[b], sin));
+    // the layer: needs its tokens, and output buffer b drained (i-2 copied out)
+    MOE_CUDA(cudaStreamWaitEvent(sc, ev_in[b], 0));
+    if (i >= 2) MOE_CUDA(cudaStreamWaitEvent(sc, ev_out[b], 0));
+    MOE_TRY(moe_layer_fwd(s, xbuf[b], gate, gate_bias, W1, W2, ybuf[b], auxbuf[b], nullptr,
+                          nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dev_status, ws,
+                          layer_bytes, sc, nullptr));
+    MOE_CUDA(cudaEventRecord(ev_layer[b], sc));
+    // outputs out
+    MOE_CUDA(cudaStreamWaitEvent(sout, ev_layer[b], 0));
+    if (tok_bytes)
+      MOE_CUDA(cudaMemcpyAsync(y_host[i], ybuf[b], tok_bytes, cudaMemcpyDeviceToHost, sout));
+    if (aux_host)
+      MOE_CUDA(cudaMemcpyAsync(aux_host + i, auxbuf[b], sizeof(float), cudaMemcpyDeviceToHost, sout));
+    MOE_CUDA(cudaEventRecord(ev_out[b], sout));
+  }
+  return MOE_OK;
+}
+
 }  // extern "C"
