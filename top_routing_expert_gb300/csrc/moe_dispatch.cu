@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
   const int nvec = a.H >> 3;  // 16-byte vectors per row
   const uint4* __restrict__ xv = reinterpret_cast<const uint4*>(a.x);
   uint4* __restrict__ pv = reinterpret_cast<uint4*>(a.x_perm);
+  const int64_t rows = static_cast<int64_t>(a.T) * a.k;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
     int e = -1;
     if (lane < a.k) e = a.topk_idx[static_cast<size_t>(t) * a.k + lane];
@@ -144,7 +145,10 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
     if (ok) {
       const int64_t pos = static_cast<int64_t>(a.tile_base[static_cast<size_t>(e) * a.n_tiles + t / kTileTokens]) +
                           a.rank8[static_cast<size_t>(t) * a.k + lane];
-      if (pos < a.C) dest = a.offsets[e] + static_cast<int>(pos);
+      const int64_t row = static_cast<int64_t>(a.offsets[e]) + pos;
+      // rows outside the buffer can only come from routing state left
+      // incomplete by an aborted kernel (MOE_DEV_TIMEOUT): never written
+      if (pos >= 0 && pos < a.C && row >= 0 && row < rows) dest = static_cast<int>(row);
     }
     if (lane < a.k) {
       a.dest_row[static_cast<size_t>(t) * a.k + lane] = dest;

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             s = S - 1;
             ph ^= 1u;
           }
-          mbar_wait_drain(&full[s], ph, 100000000ull);
+          mbar_wait_drain(&full[s], ph, kDrainLimitNs);
         }
       }
     }
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // every UMMA issued must finish before TMEM is released
       umma_commit(drain);
-      mbar_wait_drain(drain, 0, 100000000ull);
+      mbar_wait_drain(drain, 0, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------ epilogue ----

@@ -179,16 +179,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (aborted && leader) {
-        // let the last loads issued land before the CTA exits
-        int s = stage;
-        uint32_t ph = phase;
-        for (int d = 0; d < kStages && d < issued; ++d) {
-          if (--s < 0) {
-            s = kStages - 1;
-            ph ^= 1u;
+      if (aborted) {
+        if (leader) {
+          // let the last loads issued land before the CTA exits (the leader's
+          // barriers count both CTAs' bytes)
+          int s = stage;
+          uint32_t ph = phase;
+          for (int d = 0; d < kStages && d < issued; ++d) {
+            if (--s < 0) {
+              s = kStages - 1;
+              ph ^= 1u;
+            }
+            mbar_wait_drain(&full[s], ph, kDrainLimitNs);
           }
-          mbar_wait_drain(&full[s], ph, 100000000ull);
+        } else {
+          // the peer's loads signal the leader's barriers, which may never
+          // be armed after an abort: give them a fixed grace period (a TMA
+          // tile lands within microseconds) before the CTA can exit
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 1000000ull) {
+          }
         }
       }
     }
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every UMMA issued must finish before TMEM is released
       umma_commit_pair(drain);
-      mbar_wait_drain(drain, 0, 100000000ull);
+      mbar_wait_drain(drain, 0, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------ epilogue ----

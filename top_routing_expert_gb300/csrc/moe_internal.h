@@ -15,6 +15,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kBlockK = 64;       // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;      // waits for in-flight copies/MMAs on abort
 
 // Router epilogue arguments (GEMM and logits entry points).
 struct RouteArgs {

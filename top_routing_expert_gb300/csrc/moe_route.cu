@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
     if (kb < nk) {
       // aborted: let the loads already issued land before the CTA exits
       for (int d = (kb > S ? kb - S : 0); d < kb; ++d)
-        mbar_wait_drain(&sm.full[d % S], (d / S) & 1, 100000000ull);
+        mbar_wait_drain(&sm.full[d % S], (d / S) & 1, kDrainLimitNs);
     }
   } else if (warp == 1 && lane == 0) {
     // UMMA issuer: D[128 x E_pad] += X[128 x 64] * gate^T[64 x E_pad] per stage
@@ -437,7 +437,10 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
 
   // all threads: wait for the accumulator, then the routing epilogue (the
   // decision is made CTA-uniform because the epilogue synchronises)
-  const bool done_ok = mbar_wait_drain(sm.done, 0, 4ull * a.timeout_ns);
+  // `done` is committed even on abort and fires once the issued UMMAs are
+  // finished, which TMEM release must wait for: a fixed drain limit, not
+  // the (caller-settable) pipeline timeout.
+  const bool done_ok = mbar_wait_drain(sm.done, 0, kDrainLimitNs);
   const int go = __syncthreads_and(done_ok && *sm.abort_flag == 0u);
   tc_fence_after();
   if (go) {
