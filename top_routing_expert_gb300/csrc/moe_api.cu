@@ -251,7 +251,7 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
     // 256-column row pieces (512 B), used only for L2 prefetch
     if (!tmap_bf16_2d(&tm_rows, x, d.H, d.T, 256, kTileTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
       return MOE_ERR_CUDA;
-    MOE_CUDA(launch_route_gemm(tm_x, tm_g, tm_rows, a, st));
+    MOE_CUDA(launch_route_gemm(tm_x, tm_g, tm_rows, a, st, num_sms()));
   }
   return MOE_OK;
 }

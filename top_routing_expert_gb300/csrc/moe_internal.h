@@ -103,7 +103,8 @@ size_t gemm_smem_bytes(int E);
 cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, int E, int E_pad,
                                   cudaStream_t st);
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st);
+                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st,
+                              int num_sms);
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st);
 cudaError_t launch_rank(const RankArgs& a, cudaStream_t st);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);

@@ -168,11 +168,30 @@ __device__ __forceinline__ EpiScratch carve_epi(uint8_t* p, int npart, int kmax)
 //   5. in-tile arrival ranks and per-tile expert counts from warp bit masks;
 //   6. per-expert sums of p over the tile's tokens (fixed butterfly per warp,
 //      then quadrants in order).
-template <int KMAX, class Src>
+// The epilogue's thread group: the whole CTA (synchronised by
+// __syncthreads) or, in the persistent router, the epilogue warps only
+// (named barrier 1), numbered from `first_thread`.
+struct CtaGroup {
+  __device__ __forceinline__ int tid() const { return threadIdx.x; }
+  __device__ __forceinline__ int size() const { return blockDim.x; }
+  __device__ __forceinline__ void sync() const { __syncthreads(); }
+};
+
+struct WarpGroup {
+  int first_thread, nthreads;
+  __device__ __forceinline__ int tid() const { return threadIdx.x - first_thread; }
+  __device__ __forceinline__ int size() const { return nthreads; }
+  __device__ __forceinline__ void sync() const {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  }
+};
+
+template <int KMAX, class Src, class Group>
 __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& a, int tile,
                                                EpiScratch es, uint32_t* masks, float* red,
-                                               int E_stride, int npart, int cpt) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+                                               int E_stride, int npart, int cpt,
+                                               const Group& grp) {
+  const int tid = grp.tid(), lane = tid & 31, warp = tid >> 5;
   const int q = warp & 3, part = warp >> 2;
   const int r = 32 * q + lane;
   const int E = a.E, k = a.k;
@@ -205,7 +224,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
     es.cand_v[cbase + j] = tk.v[j];
     es.cand_i[cbase + j] = tk.i[j];
   }
-  __syncthreads();
+  grp.sync();
   if (part == 0) {
 #pragma unroll 1
     for (int pp = 1; pp < npart; ++pp) {
@@ -216,7 +235,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
     }
     es.rowmax[r] = tk.v[0];
   }
-  __syncthreads();
+  grp.sync();
   const float m = es.rowmax[r];
   float s_loc = 0.f;
 #pragma unroll 1
@@ -228,7 +247,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
       if (c + i < E) s_loc += expf(v[i] - m);
   }
   es.psum[r * npart + part] = s_loc;
-  __syncthreads();
+  grp.sync();
 
   int eid[KMAX];
   float ex[KMAX];
@@ -246,7 +265,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
       if (valid && eid[j] >= 0) atomicOr(&masks[q * E_stride + eid[j]], 1u << lane);
     }
   }
-  __syncthreads();
+  grp.sync();
 
   // per-expert probability sums over the tile's tokens
   const float inv_s = 1.0f / es.rowsum[r];
@@ -284,14 +303,14 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
     }
   }
   if (bad && valid) atomicOr(a.dev_status, MOE_DEV_NONFINITE);
-  for (int x = tid; x < E; x += blockDim.x) {
+  for (int x = tid; x < E; x += grp.size()) {
     int c = 0;
 #pragma unroll
     for (int w = 0; w < kTileTokens / 32; ++w) c += __popc(masks[w * E_stride + x]);
     a.tile_cnt[static_cast<size_t>(x) * a.n_tiles + tile] = c;
   }
-  __syncthreads();
-  for (int x = tid; x < E; x += blockDim.x) {
+  grp.sync();
+  for (int x = tid; x < E; x += grp.size()) {
     float sum = red[x];
 #pragma unroll
     for (int w = 1; w < kTileTokens / 32; ++w) sum += red[w * E_stride + x];
@@ -447,13 +466,232 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
     TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s};
     // the pipeline stages are free now: they hold the epilogue scratch
     route_epilogue<KMAX>(src, a, tile, carve_epi(smem, npart, KMAX), sm.masks, sm.red, E32,
-                         npart, cpt);
+                         npart, cpt, CtaGroup{});
   } else if (tid == 0) {
     atomicOr(a.dev_status, MOE_DEV_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
+// Persistent router: one CTA per SM takes tiles blockIdx.x, +gridDim.x, ...
+// Warp 0 streams x and the gate through the stage ring across tile
+// boundaries, warp 1 issues the UMMAs into one of two TMEM accumulators,
+// and 4 * npart epilogue warps (warps 4..) route the previous tile from the
+// other accumulator meanwhile, synchronising among themselves only.
+constexpr int kPersistParts = 4;
+
+__host__ __device__ inline int persist_parts_of(int E) {
+  const int n = route_parts_of(E);
+  return n > kPersistParts ? kPersistParts : n;
+}
+__host__ __device__ inline int persist_cpt_of(int E) {
+  const int n = persist_parts_of(E);
+  return ((E + n - 1) / n + kChunk - 1) / kChunk * kChunk;
+}
+
+struct PersistLayout {
+  int S, npart, cpt, E32;
+  uint32_t stage_bytes, ncols;
+  size_t off_bar, off_bias, off_masks, off_red, off_epi, total;
+};
+
+__host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int kmax) {
+  PersistLayout L;
+  L.npart = persist_parts_of(E);
+  L.cpt = persist_cpt_of(E);
+  const int ecols = L.npart * L.cpt;
+  L.E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
+  L.stage_bytes = static_cast<uint32_t>(kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2);
+  int c = 32;
+  while (c < 2 * L.E32) c <<= 1;
+  L.ncols = static_cast<uint32_t>(c);
+  const size_t fixed = 8 * 24 + 16 + static_cast<size_t>(L.E32) * 4 * 9 + epi_scratch_bytes(L.npart, kmax);
+  int S = static_cast<int>((225 * 1024 - 1024 - fixed) / L.stage_bytes);
+  L.S = S > 8 ? 8 : S;
+  L.off_bar = static_cast<size_t>(L.S) * L.stage_bytes;
+  L.off_bias = L.off_bar + 8 * (2 * L.S + 5) + 16;
+  L.off_masks = L.off_bias + 4 * L.E32;
+  L.off_red = L.off_masks + 16 * L.E32;
+  L.off_epi = L.off_red + 16 * L.E32;
+  L.total = 1024 + L.off_epi + epi_scratch_bytes(L.npart, kmax);
+  return L;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
+    route_persistent_kernel(const __grid_constant__ CUtensorMap tm_x,
+                            const __grid_constant__ CUtensorMap tm_gate,
+                            const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_up_1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX);
+  const int S = L.S, E32 = L.E32;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* abort_flag = tmem_slot + 1;
+  float* bias_s = reinterpret_cast<float*>(smem + L.off_bias);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L.off_masks);
+  float* red = reinterpret_cast<float*>(smem + L.off_red);
+  const EpiScratch es = carve_epi(smem + L.off_epi, L.npart, KMAX);
+  const int n_epi = kTileTokens * L.npart;
+  const uint32_t a_bytes = kTileTokens * kBlockK * 2;
+
+  if (blockIdx.x == 0 && tid == 0) *a.ticket = 0u;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, L.ncols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], n_epi);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 2 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_gate);
+  }
+  for (int i = tid; i < E32; i += blockDim.x)
+    bias_s[i] = (a.bias != nullptr && i < a.E) ? a.bias[i] : 0.f;
+  for (int i = tid; i < 4 * E32; i += blockDim.x) masks[i] = 0u;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, a.dev_status, a.timeout_ns};
+  const int nk = a.H / kBlockK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer ----
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool aborted = false;
+      const int n_groups = (nk + kRowGroup - 1) / kRowGroup;
+      for (int tile = blockIdx.x; tile < a.n_tiles && !aborted; tile += gridDim.x) {
+        for (int g = 0; g < kRouteGroupsAhead && g < n_groups; ++g)
+          tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+            aborted = true;
+            break;
+          }
+          uint8_t* st = smem + static_cast<size_t>(stage) * L.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
+          tma_load_2d(st, &tm_x, &full[stage], kb * kBlockK, tile * kTileTokens);
+          tma_load_2d(st + a_bytes, &tm_gate, &full[stage], kb * kBlockK, 0);
+          if (kb % kRowGroup == 0) {
+            const int g = kb / kRowGroup + kRouteGroupsAhead;
+            if (g < n_groups)
+              tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        int s = stage;
+        uint32_t ph = phase;
+        for (int d = 0; d < S && d < issued; ++d) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1u;
+          }
+          mbar_wait_drain(&full[s], ph, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------- UMMA issuer ----
+      const uint32_t idesc =
+          idesc_bf16_f32(kTileTokens, static_cast<uint32_t>(a.E_pad), false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < a.n_tiles && !aborted; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * E32);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(stage) * L.stage_bytes);
+          const uint32_t b_addr = a_addr + a_bytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // TMEM is released only after every issued UMMA is done
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, kDrainLimitNs);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------- epilogue ----
+    const WarpGroup grp{kTileTokens, n_epi};
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      tc_fence_after();
+      TmemSource src{tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * E32),
+                     bias_s};
+      route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, L.npart, L.cpt, grp);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      // clear the bit masks for the next tile (ordered before its use by the
+      // next tile's first group barrier)
+      for (int i = grp.tid(); i < 4 * E32; i += n_epi) masks[i] = 0u;
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, L.ncols);
 }
 
 template <int KMAX>
@@ -471,7 +709,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1) route_logits_kernel(RouteA
   __syncthreads();
   const int t = tile * kTileTokens + 32 * (warp & 3) + lane;
   GlobalSource src{a.logits_in + static_cast<size_t>(t < a.T ? t : 0) * a.E, a.E, t < a.T};
-  route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, npart, cpt);
+  route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, npart, cpt, CtaGroup{});
 }
 
 // Tile counts and ranks from caller-given indices. A slot is unusable if its
@@ -561,8 +799,35 @@ cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_g
   return cudaGetLastError();
 }
 
+template <int KMAX>
+cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
+                                      const CUtensorMap& tm_x_rows, const RouteArgs& a,
+                                      int num_sms, cudaStream_t st) {
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX);
+  if (L.S < 2) return cudaErrorInvalidConfiguration;
+  cudaError_t err = cudaFuncSetAttribute(route_persistent_kernel<KMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L.total));
+  if (err != cudaSuccess) return err;
+  const int grid = a.n_tiles < num_sms ? a.n_tiles : num_sms;
+  route_persistent_kernel<KMAX><<<grid, kTileTokens + kTileTokens * L.npart, L.total, st>>>(
+      tm_x, tm_gate, tm_x_rows, a);
+  return cudaGetLastError();
+}
+
+bool route_use_persistent(const RouteArgs& a, int num_sms) {
+  return a.n_tiles >= 3 * num_sms;
+}
+
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st,
+                              int num_sms) {
+  if (route_use_persistent(a, num_sms)) {
+    if (a.k <= 2) return launch_route_persistent_k<2>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
+    if (a.k <= 4) return launch_route_persistent_k<4>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
+    if (a.k <= 6) return launch_route_persistent_k<6>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
+    return launch_route_persistent_k<8>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
+  }
   if (a.k <= 2) return launch_route_gemm_k<2>(tm_x, tm_gate, tm_x_rows, a, st);
   if (a.k <= 4) return launch_route_gemm_k<4>(tm_x, tm_gate, tm_x_rows, a, st);
   if (a.k <= 6) return launch_route_gemm_k<6>(tm_x, tm_gate, tm_x_rows, a, st);
