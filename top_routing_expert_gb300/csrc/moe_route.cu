@@ -475,7 +475,8 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   if (warp == 0) tmem_dealloc(tmem, ncols);
 }
 
-// Persistent router: one CTA per SM takes tiles blockIdx.x, +gridDim.x, ...
+// Persistent router (used when there are more tiles than SMs): one CTA per
+// SM takes tiles blockIdx.x, +gridDim.x, ...
 // Warp 0 streams x and the gate through the stage ring across tile
 // boundaries, warp 1 issues the UMMAs into one of two TMEM accumulators,
 // and 4 * npart epilogue warps (warps 4..) route the previous tile from the
@@ -816,7 +817,7 @@ cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap
 }
 
 bool route_use_persistent(const RouteArgs& a, int num_sms) {
-  return a.n_tiles >= 3 * num_sms;
+  return a.n_tiles > num_sms;
 }
 
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
