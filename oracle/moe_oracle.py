@@ -41,6 +41,8 @@ R6  Within an expert, assignments are served in token order and those at
 R7  Expert FFN: act = bf16(gelu_tanh(x W1_e)); y_e = bf16(act W2_e), no
     biases (the module notes' 4.2 listing has bias-free expert weights).
 R8  Combine: y[t] = bf16( sum over kept slots, ascending j, of w[t,j] y_e ).
+R11 Training router (Gumbel): z = (logits + g)/tau with g from caller-drawn
+    uniforms; top-k on z, weights and balance statistics from softmax(z).
 
 Parity pins for every function here live in tests/test_oracle_pins.py.
 """
@@ -142,6 +144,28 @@ def route_from_logits(logits: np.ndarray, k: int) -> Routing:
     """Softmax, top-k and renormalise, in that order (R1-R3)."""
     p = softmax(logits)
     idx = topk(logits, k)
+    return Routing(idx=idx, w=renormalise(p, idx), p=p)
+
+
+def gumbel_noise(u: np.ndarray) -> np.ndarray:
+    """Gumbel noise from uniforms u in [0, 1): g = -log(-log(u + 1e-9) + 1e-9)
+    (module notes 3.1 router listing and the 4.2 MoELayer listing; the 1e-9
+    terms keep both logarithms finite)."""
+    u = np.asarray(u, np.float64)
+    return -np.log(-np.log(u + 1e-9) + 1e-9)
+
+
+def route_gumbel(logits: np.ndarray, u: np.ndarray, temperature: float, k: int) -> Routing:
+    """The training router (module notes 3.1): z = (logits + g) / temperature,
+    p = softmax(z), top-k of z (the same set as top-k of p), weights p
+    renormalised over the k chosen (R11: the balance statistics then use this
+    perturbed p, as the 4.2 listing feeds `probs` to its balance loss)."""
+    z = (np.asarray(logits, np.float64) + gumbel_noise(u)) / float(temperature)
+    if not np.all(np.isfinite(z)):
+        raise ValueError("router scores must be finite")
+    zz = np.exp(z - z.max(axis=1, keepdims=True))
+    p = zz / zz.sum(axis=1, keepdims=True)
+    idx = np.argsort(-z, axis=1, kind="stable")[:, :k].astype(np.int32)
     return Routing(idx=idx, w=renormalise(p, idx), p=p)
 
 

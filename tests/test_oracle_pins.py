@@ -137,6 +137,51 @@ def test_renormalised_weights():
             assert np.allclose(np.take_along_axis(r.p, r.idx.astype(np.int64), 1), r.w, atol=1e-15)
 
 
+def test_gumbel_noise_closed_forms():
+    # g(u) = -log(-log(u)) up to the 1e-9 guards: g = 0 at u = 1/e, and g is
+    # increasing; its mean over uniforms is the Euler-Mascheroni constant
+    assert abs(O.gumbel_noise(np.array([math.exp(-1.0) - 1e-9]))[0]) < 1e-8
+    u = np.sort(rng.random(1000))
+    assert (np.diff(O.gumbel_noise(u)) >= 0).all()
+    big = rng.random(2_000_000)
+    assert abs(O.gumbel_noise(big).mean() - 0.5772156649) < 0.005
+
+
+def test_gumbel_router_reduces_to_plain_router_without_noise():
+    lg = rng.standard_normal((200, 9)).astype(np.float32)
+    u = np.full(lg.shape, math.exp(-1.0) - 1e-9)         # g = 0
+    for k in (1, 3):
+        g = O.route_gumbel(lg, u, 1.0, k)
+        r = O.route_from_logits(lg, k)
+        assert np.array_equal(g.idx, r.idx)
+        assert np.allclose(g.w, r.w, atol=1e-12)
+        assert np.allclose(g.p, r.p, atol=1e-12)
+
+
+def test_gumbel_router_temperature():
+    lg = rng.standard_normal((300, 7)).astype(np.float32)
+    u = rng.random(lg.shape)
+    base = O.route_gumbel(lg, u, 1.0, 3)
+    for tau in (0.25, 4.0):
+        r = O.route_gumbel(lg, u, tau, 3)
+        assert np.array_equal(r.idx, base.idx)          # order is unchanged by tau > 0
+        z = (lg.astype(np.float64) + O.gumbel_noise(u)) / tau
+        assert np.allclose(np.log(r.p[:, 0] / r.p[:, 1]), z[:, 0] - z[:, 1], atol=1e-9)
+    # a high temperature flattens p towards uniform
+    assert np.abs(O.route_gumbel(lg, u, 1e6, 3).p - 1 / 7).max() < 1e-5
+
+
+def test_gumbel_max_selects_with_softmax_probabilities():
+    # the Gumbel-max trick: argmax(logits + g) is a sample from softmax(logits)
+    lg = np.array([[1.5, 0.0, -0.7, 0.3]], np.float32)
+    n = 200_000
+    u = rng.random((n, 4))
+    r = O.route_gumbel(np.repeat(lg, n, axis=0), u, 1.0, 1)
+    freq = np.bincount(r.idx[:, 0], minlength=4) / n
+    p = O.softmax(lg)[0]
+    assert np.abs(freq - p).max() < 4 * np.sqrt(p * (1 - p) / n).max()
+
+
 def test_nonfinite_logits_rejected():
     lg = np.zeros((2, 4), np.float32)
     lg[1, 2] = np.nan
