@@ -142,10 +142,21 @@ def run_ours(args, rank, world, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(events=None):
-        moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux,
-                          offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
-                          stream=stream, events=events)
+    if args.gumbel is None:
+        def step(events=None):
+            moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux,
+                              offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
+                              stream=stream, events=events)
+    else:
+        # the training router: uniforms drawn once, outside the timed region
+        gen = torch.Generator(device=dev).manual_seed(rank + 1)
+        noise = torch.rand((T, E), generator=gen, device=dev, dtype=torch.float32)
+
+        def step(events=None):
+            moe.moe_layer_fwd_gumbel(s, d["x"], d["gate"], d["bias"], noise, args.gumbel,
+                                     d["W1"], d["W2"], y, aux=aux, offsets=offsets,
+                                     dest_row=dest, dev_status=status, ws=ws, stream=stream,
+                                     events=events)
 
     for _ in range(args.warmup):
         step()
@@ -193,7 +204,9 @@ def run_ours(args, rank, world, local_rank):
     n_kept = int(offsets[E].item())
     any_kept = int((dest >= 0).any(dim=1).sum().item())
 
-    e2e = None if args.no_e2e else run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
+    # the end-to-end leg times the inference layer; skipped for the training router
+    e2e = None if (args.no_e2e or args.gumbel is not None) else \
+        run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
     if rank != 0:
         return None
     l2 = (f"L2 flushed between steps ({2 * L2_BYTES >> 20} MB write); steps timed by their own events"
@@ -274,6 +287,8 @@ def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "parallelism": f"replicas x{world} (no exchange)",
+                   "router": "inference (top-k of logits)" if args.gumbel is None
+                   else f"training (Gumbel noise, temperature {args.gumbel})",
                    "l2": l2},
         "clocks": clk,
         "e2e": None if e2e is None else {
@@ -366,6 +381,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gumbel", type=float, default=None, metavar="TAU",
+                    help="time the layer with the Gumbel training router at temperature TAU")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

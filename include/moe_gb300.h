@@ -46,6 +46,13 @@
 extern "C" {
 #endif
 
+/* Exported symbols of the shared library (everything else is hidden). */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 #define MOE_GB300_ABI_VERSION 1
 
 typedef uint16_t moe_bf16; /* a bf16 value as its 16 bits */
@@ -84,18 +91,18 @@ typedef enum {
  * notes' listing, section 4.2, counts tokens as T*k and floors C at 1).
  * Returns -1 for E < 1, k < 1, T < 0 or a non-finite/non-positive cf.
  * Host only; needs no GPU. */
-int64_t moe_capacity(int64_t T, int64_t E, int64_t top_k, double capacity_factor);
+MOE_API int64_t moe_capacity(int64_t T, int64_t E, int64_t top_k, double capacity_factor);
 
 /* Bytes of device workspace any entry point needs for this shape (one size
  * serves all of them). Host only. Returns MOE_ERR_NULL / _SHAPE /
  * _UNSUPPORTED for bad arguments. */
-moe_status moe_workspace_size(const moe_shape* s, size_t* bytes);
+MOE_API moe_status moe_workspace_size(const moe_shape* s, size_t* bytes);
 
 /* Static text for a status code. Host only. */
-const char* moe_status_str(moe_status st);
+MOE_API const char* moe_status_str(moe_status st);
 
 /* MOE_GB300_ABI_VERSION of the built library. Host only. */
-int moe_abi_version(void);
+MOE_API int moe_abi_version(void);
 
 /* Router: logits GEMM on the tensor cores, softmax, top-k, renormalised
  * weights and the load-balancing statistics (MoE module notes, section 3.1
@@ -108,7 +115,7 @@ int moe_abi_version(void);
  *        (E * sum_e routed_e/(T*k) * P_e; the loss weight alpha is the
  *        caller's), logits_out [T,E] fp32 or NULL (bias included).
  * routed_counts, P, aux may be NULL. */
-moe_status moe_route(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+MOE_API moe_status moe_route(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
                      const float* gate_bias, int32_t* topk_idx, float* topk_w,
                      int32_t* routed_counts, float* P, float* aux, float* logits_out,
                      uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
@@ -117,9 +124,26 @@ moe_status moe_route(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate
  * (the MoE module notes, section 5.2, take top-k directly on the logits at
  * inference). Same outputs and rules as moe_route; with equal logits the
  * two give identical indices, weights and statistics. */
-moe_status moe_route_logits(const moe_shape* s, const float* logits, int32_t* topk_idx,
+MOE_API moe_status moe_route_logits(const moe_shape* s, const float* logits, int32_t* topk_idx,
                             float* topk_w, int32_t* routed_counts, float* P, float* aux,
                             uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* The training router of the MoE module notes page, section 3.1: Gumbel
+ * noise is added to the logits and the sum is divided by a temperature,
+ *   scores = (x . gate + bias + g) / temperature,
+ *   g = -log(-log(u + 1e-9) + 1e-9),
+ * with u the caller's uniform draws in [0,1) (noise_u [T,E] fp32, device;
+ * the library draws no random numbers). Top-k is taken on the scores, the
+ * weights are softmax(scores) renormalised over the k chosen, and the
+ * balance statistics use softmax(scores) (the module notes feed these
+ * probabilities to their balance loss). scores_out [T,E] fp32 or NULL
+ * receives the scores. temperature must be finite and > 0. Other arguments
+ * as moe_route. */
+MOE_API moe_status moe_route_gumbel(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                            const float* gate_bias, const float* noise_u, float temperature,
+                            int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                            float* aux, float* scores_out, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /* Dispatch: capacity-bounded, token-ordered permutation of token rows into
  * expert-major order - the single-GPU form of the dispatch all-to-all (MoE
@@ -132,7 +156,7 @@ moe_status moe_route_logits(const moe_shape* s, const float* logits, int32_t* to
  *        x_perm [T*k,H] bf16 (row dest_row[t,j] = x[t]).
  * kept_counts, src_token may be NULL. Bad or repeated indices set
  * MOE_DEV_BAD_INDEX / MOE_DEV_DUP_INDEX and that slot is dropped. */
-moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+MOE_API moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
                        int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
                        int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status,
                        void* ws, size_t ws_bytes, void* stream);
@@ -144,7 +168,7 @@ moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* top
  *   in : x_perm [T*k,H] bf16, offsets [E+1] int32, W1 [E,H,h], W2 [E,h,H]
  *   out: act [T*k,h] bf16 = bf16(gelu_tanh(x_perm . W1[e])) (fp32 accumulate),
  *        y_perm [T*k,H] bf16 = bf16(act . W2[e]). */
-moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int32_t* offsets,
+MOE_API moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int32_t* offsets,
                           const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
                           moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
                           void* stream);
@@ -154,7 +178,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int3
  * y[t] = bf16(sum_{j: dest_row[t,j] >= 0, ascending j} topk_w[t,j] *
  * y_perm[dest_row[t,j]]), fp32 accumulation; a token with no kept slot gets
  * zeros. Needs no workspace. */
-moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t* dest_row,
+MOE_API moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t* dest_row,
                        const float* topk_w, moe_bf16* y, void* stream);
 
 /* The whole layer forward: route, dispatch, expert FFN and combine on one
@@ -166,17 +190,28 @@ moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t
  *        pointer to an array); events[0] is recorded before the first
  *        kernel and events[1..6] after the route, scan, permute, FFN GEMM1,
  *        FFN GEMM2 and combine stages, for per-stage timing. */
-moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+MOE_API moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
                          const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
                          moe_bf16* y, float* aux, int32_t* topk_idx, float* topk_w,
                          int32_t* routed_counts, float* P, int32_t* kept_counts,
                          int32_t* offsets, int32_t* dest_row, uint32_t* dev_status,
                          void* ws, size_t ws_bytes, void* stream, void* const* events);
 
+/* moe_layer_fwd with the training router of moe_route_gumbel (Gumbel noise
+ * from the caller's uniforms noise_u [T,E], temperature > 0); events as in
+ * moe_layer_fwd. */
+MOE_API moe_status moe_layer_fwd_gumbel(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                                const float* gate_bias, const float* noise_u, float temperature,
+                                const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y, float* aux,
+                                int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                                int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events);
+
 /* Bytes of device workspace moe_layer_fwd_host needs for micro-batches of
  * this shape: the layer workspace plus two token and two output buffers.
  * Host only. */
-moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes);
+MOE_API moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes);
 
 /* Host-to-host layer forward over n_micro micro-batches of s->T tokens each,
  * pipelined over three caller streams - the dual-stream, micro-batch overlap
@@ -198,7 +233,7 @@ moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes);
  *        disabled); they order the buffers between the streams.
  * Everything is enqueued and the call returns; y_host and aux_host are valid
  * once streams[2] has completed. */
-moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
+MOE_API moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
                               moe_bf16* const* y_host, float* aux_host, const moe_bf16* gate,
                               const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
                               uint32_t* dev_status, void* ws, size_t ws_bytes,
@@ -217,7 +252,7 @@ moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf1
  *     device); make it before any stream capture.
  *   - All calls on a device share the array; calls that overlap on the GPU
  *     race and must be serialised by the caller. Allocates nothing. */
-moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+MOE_API moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
                                int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
                                int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status,
                                void* stream);

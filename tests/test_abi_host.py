@@ -38,6 +38,40 @@ def test_header_declares_the_abi():
     assert set(names) == set(moe.EXPORTED_SYMBOLS)
 
 
+def declared_signatures():
+    """{name: [parameter type strings]} from the header's declarations."""
+    text = ""
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text += open(os.path.join(inc, f)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    sigs = {}
+    for m in re.finditer(r"\b(moe_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        if params == ["void"]:
+            params = []
+        sigs[m.group(1)] = params
+    return sigs
+
+
+def test_binding_argument_lists_match_the_header(lib):
+    # every ctypes prototype has the header's arity, and scalars keep their C type
+    kinds = {"int64_t": ctypes.c_int64, "double": ctypes.c_double, "float": ctypes.c_float,
+             "size_t": ctypes.c_size_t}
+    sigs = declared_signatures()
+    assert set(sigs) == set(moe.EXPORTED_SYMBOLS)
+    for name, params in sigs.items():
+        argtypes = getattr(lib, name).argtypes or []
+        assert len(argtypes) == len(params), (name, len(argtypes), params)
+        for p, t in zip(params, argtypes):
+            base = p.replace("const", "").split()[0] if "*" not in p else None
+            if base in kinds:
+                assert t is kinds[base], (name, p, t)
+            elif "*" in p:
+                assert t is not ctypes.c_float and t is not ctypes.c_double, (name, p, t)
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
         assert hasattr(lib, n), n

@@ -508,3 +508,81 @@ def test_layer_host_pipeline_equals_device_layer():
         torch.cuda.synchronize()
         assert torch.equal(y.cpu(), y_host[i]), i
         assert float(aux.item()) == float(aux_host[i])
+
+
+# ============================================================ Gumbel router
+
+def _uniforms(T, E, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return torch.rand((T, E), generator=gen, dtype=torch.float32)
+
+
+@pytest.mark.parametrize("T,H,E,k,tau", [(1000, 512, 12, 3, 1.0), (777, 256, 64, 6, 0.5),
+                                         (300, 1024, 8, 2, 2.0), (5000, 256, 128, 2, 1.0)])
+def test_route_gumbel_against_oracle(T, H, E, k, tau):
+    gen = torch.Generator().manual_seed(T + E)
+    x = torch.randn((T, H), generator=gen).to(torch.bfloat16)
+    gate = (torch.randn((H, E), generator=gen) / H ** 0.5).to(torch.bfloat16)
+    b = torch.randn(E, generator=gen) * 0.5
+    u = _uniforms(T, E, seed=T)
+    s = _shape(T, H, E, k, 64, 1.0)
+    ws = moe.Workspace(s)
+    idx = _zeros((T, k), torch.int32)
+    w = _zeros((T, k), torch.float32)
+    routed = _zeros(E, torch.int32)
+    P = _zeros(E, torch.float32)
+    aux = _zeros(1, torch.float32)
+    sc = _zeros((T, E), torch.float32)
+    st = _status()
+    moe.moe_route_gumbel(s, x.to(DEV), gate.to(DEV), b.to(DEV), u.to(DEV), tau, idx, w, routed,
+                         P, aux, sc, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lg = oracle_logits_chunked(x, gate, b)
+    r = O.route_gumbel(lg, u.numpy(), tau, k)
+    z = (lg.astype(np.float64) + O.gumbel_noise(u.numpy())) / tau
+    assert np.abs(sc.cpu().numpy() - z).max() <= 1e-4 * (1 + np.abs(z).max())
+    gidx = idx.cpu().numpy()
+    mism = np.nonzero((gidx != r.idx).any(axis=1))[0]
+    assert (topk_margins(z, k)[mism] < NEAR_TIE * (1 + np.abs(z).max())).all()
+    ok = np.setdiff1d(np.arange(T), mism)
+    assert np.abs(w.cpu().numpy()[ok] - r.w[ok]).max() <= 1e-5
+    stt = O.load_balance_stats(r.idx, r.p, E)
+    if len(mism) == 0:
+        assert np.array_equal(routed.cpu().numpy(), stt.routed)
+        assert abs(float(aux.item()) - stt.aux) <= 1e-4 * stt.aux
+    assert np.allclose(P.cpu().numpy(), stt.P, rtol=1e-4, atol=1e-6)
+
+
+def test_layer_gumbel_against_oracle():
+    w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="gumbel_layer")
+    inp = W.make_inputs(w, seed=31)
+    u = _uniforms(w.T, w.E, seed=32)
+    tau = 0.7
+    s = _shape(w.T, w.H, w.E, w.k, w.h, w.cf)
+    ws = moe.Workspace(s)
+    y = _zeros((w.T, w.H), torch.bfloat16)
+    idx = _zeros((w.T, w.k), torch.int32)
+    dest = _zeros((w.T, w.k), torch.int32)
+    st = _status()
+    dv = {n: v.to(DEV) for n, v in inp.items() if v is not None}
+    moe.moe_layer_fwd_gumbel(s, dv["x"], dv["gate"], dv["bias"], u.to(DEV), tau, dv["W1"], dv["W2"],
+                             y, topk_idx=idx, dest_row=dest, dev_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lg = oracle_logits_chunked(inp["x"], inp["gate"], inp["bias"])
+    r = O.route_gumbel(lg, u.numpy(), tau, w.k)
+    d = O.dispatch_plan(r.idx, w.E, O.capacity(w.T, w.E, w.k, w.cf))
+    gidx = idx.cpu().numpy()
+    z = (lg.astype(np.float64) + O.gumbel_noise(u.numpy())) / tau
+    mism = np.nonzero((gidx != r.idx).any(axis=1))[0]
+    assert (topk_margins(z, w.k)[mism] < NEAR_TIE * (1 + np.abs(z).max())).all()
+    if len(mism) == 0:
+        assert np.array_equal(dest.cpu().numpy(), d.dest_row)
+    rows = np.arange(w.T)
+    same = (gidx == r.idx).all(1) & ((dest.cpu().numpy() >= 0) == (d.dest_row >= 0)).all(1)
+    rows = rows[same]
+    kept = d.dest_row[rows] >= 0
+    ref = O.token_outputs(np64(inp["x"][torch.from_numpy(rows)]), r.idx[rows], r.w[rows], kept,
+                          _Lazy64(inp["W1"]), _Lazy64(inp["W2"]))
+    assert_ffn_close(np64(y.cpu()[torch.from_numpy(rows)]), ref, "gumbel layer y")

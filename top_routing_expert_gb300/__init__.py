@@ -21,7 +21,8 @@ __all__ = [
     "MoeError", "MoeShape", "load_library", "capacity", "workspace_size", "status_str",
     "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
-    "host_workspace_size", "HostPipeline", "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
+    "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
+    "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
 
@@ -30,7 +31,8 @@ LAYER_NUM_EVENTS = 7
 EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "moe_status_str",
                     "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
                     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc",
-                    "moe_host_workspace_size", "moe_layer_fwd_host"]
+                    "moe_host_workspace_size", "moe_layer_fwd_host", "moe_route_gumbel",
+                    "moe_layer_fwd_gumbel"]
 
 
 class MoeError(RuntimeError):
@@ -84,6 +86,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_layer_fwd.argtypes = [S] + [_P] * 16 + [ctypes.c_size_t, _P, _P]
     lib.moe_permute_noalloc.restype = ctypes.c_int
     lib.moe_permute_noalloc.argtypes = [S] + [_P] * 9
+    lib.moe_route_gumbel.restype = ctypes.c_int
+    lib.moe_route_gumbel.argtypes = [S] + [_P] * 4 + [ctypes.c_float] + [_P] * 8 + [ctypes.c_size_t, _P]
+    lib.moe_layer_fwd_gumbel.restype = ctypes.c_int
+    lib.moe_layer_fwd_gumbel.argtypes = [S] + [_P] * 4 + [ctypes.c_float] + [_P] * 13 + [ctypes.c_size_t, _P, _P]
     lib.moe_host_workspace_size.restype = ctypes.c_int
     lib.moe_host_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_layer_fwd_host.restype = ctypes.c_int
@@ -164,6 +170,14 @@ def _ws(ws: Workspace | None, shape: MoeShape):
     return ws.ptr, ws.nbytes
 
 
+def _events(events):
+    if events is None:
+        return None
+    if len(events) != LAYER_NUM_EVENTS:
+        raise ValueError(f"events must hold {LAYER_NUM_EVENTS} torch.cuda.Event")
+    return (ctypes.c_void_p * LAYER_NUM_EVENTS)(*[e.cuda_event for e in events])
+
+
 # ------------------------------------------------------------ kernels ----
 
 def moe_route(shape, x, gate, gate_bias, topk_idx, topk_w, routed_counts=None, P=None,
@@ -228,11 +242,7 @@ def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None,
                   events: Optional[Sequence[torch.cuda.Event]] = None):
     s = _shape(shape)
     wp, wn = _ws(ws, s)
-    ev = None
-    if events is not None:
-        if len(events) != LAYER_NUM_EVENTS:
-            raise ValueError(f"events must hold {LAYER_NUM_EVENTS} torch.cuda.Event")
-        ev = (ctypes.c_void_p * LAYER_NUM_EVENTS)(*[e.cuda_event for e in events])
+    ev = _events(events)
     _check("moe_layer_fwd", load_library().moe_layer_fwd(
         ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
         _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
@@ -318,3 +328,39 @@ def moe_layer_fwd_host(pipeline: HostPipeline, x_host, y_host, gate, gate_bias, 
                        aux_host=None, dev_status=None):
     """C-ABI name for HostPipeline.run."""
     return pipeline.run(x_host, y_host, gate, gate_bias, W1, W2, aux_host, dev_status)
+
+
+def moe_route_gumbel(shape, x, gate, gate_bias, noise_u, temperature, topk_idx, topk_w,
+                     routed_counts=None, P=None, aux=None, scores_out=None, dev_status=None,
+                     ws: Workspace | None = None, stream=None):
+    """Training router: top-k of (x.gate + bias + gumbel(noise_u)) / temperature."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_route_gumbel", load_library().moe_route_gumbel(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(noise_u, torch.float32, "noise_u"),
+        float(temperature), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
+        _ptr(P, torch.float32, "P"), _ptr(aux, torch.float32, "aux"),
+        _ptr(scores_out, torch.float32, "scores_out"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
+
+
+def moe_layer_fwd_gumbel(shape, x, gate, gate_bias, noise_u, temperature, W1, W2, y, aux=None,
+                         topk_idx=None, topk_w=None, routed_counts=None, P=None,
+                         kept_counts=None, offsets=None, dest_row=None, dev_status=None,
+                         ws: Workspace | None = None, stream=None, events=None):
+    """moe_layer_fwd with the Gumbel training router."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    ev = _events(events)
+    _check("moe_layer_fwd_gumbel", load_library().moe_layer_fwd_gumbel(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(noise_u, torch.float32, "noise_u"),
+        float(temperature), _ptr(W1, torch.bfloat16, "W1"), _ptr(W2, torch.bfloat16, "W2"),
+        _ptr(y, torch.bfloat16, "y"), _ptr(aux, torch.float32, "aux"),
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
+        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream), ev))

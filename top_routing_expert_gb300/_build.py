@@ -31,7 +31,7 @@ def nvcc() -> str:
 
 def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
     obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
            "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]

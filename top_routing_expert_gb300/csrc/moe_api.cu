@@ -213,9 +213,14 @@ struct RouteOut {
   float* logits_out;
 };
 
+struct Noise {
+  const float* u;     // [T,E] uniforms or nullptr
+  float temperature;  // used with u
+};
+
 moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, const float* bias,
                      const float* logits_in, const RouteOut& o, uint32_t* status, const Ws& w,
-                     cudaStream_t st) {
+                     cudaStream_t st, Noise noise = Noise{nullptr, 1.0f}) {
   if (d.T == 0) {
     MOE_CUDA(cudaMemsetAsync(o.routed, 0, sizeof(int32_t) * d.E, st));
     MOE_CUDA(cudaMemsetAsync(o.P, 0, sizeof(float) * d.E, st));
@@ -231,6 +236,8 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
   a.n_tiles = d.n_tiles;
   a.stages = route_stages(d.E_pad);
   a.bias = bias;
+  a.noise_u = noise.u;
+  a.temperature = noise.temperature;
   a.logits_in = logits_in;
   a.topk_idx = o.topk_idx;
   a.topk_w = o.topk_w;
@@ -504,12 +511,12 @@ moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t
   return run_combine(d, y_perm, dest_row, topk_w, y, static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
-                         const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
-                         moe_bf16* y, float* aux, int32_t* topk_idx, float* topk_w,
-                         int32_t* routed_counts, float* P, int32_t* kept_counts,
-                         int32_t* offsets, int32_t* dest_row, uint32_t* dev_status, void* ws,
-                         size_t ws_bytes, void* stream, void* const* events) {
+static moe_status layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                     const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y,
+                     float* aux, int32_t* topk_idx, float* topk_w, int32_t* routed_counts,
+                     float* P, int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                     uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
+                     void* const* events, Noise noise) {
   MOE_TRY(check_shape(s));
   MOE_REQUIRE(x);
   MOE_REQUIRE(gate);
@@ -554,7 +561,7 @@ moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* 
     return MOE_OK;
   }
   RouteOut o{idx, wts, routed, Pp, aux, nullptr};
-  MOE_TRY(run_route(d, x, gate, gate_bias, nullptr, o, status, w, st));
+  MOE_TRY(run_route(d, x, gate, gate_bias, nullptr, o, status, w, st, noise));
   if (!mark(1)) return MOE_ERR_CUDA;
   MOE_TRY(run_scan(d, true, routed, Pp, aux, kept, off, w, st));
   if (!mark(2)) return MOE_ERR_CUDA;
@@ -567,6 +574,66 @@ moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* 
   MOE_TRY(run_combine(d, w.y_perm, dest, wts, y, st));
   if (!mark(6)) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                         const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                         moe_bf16* y, float* aux, int32_t* topk_idx, float* topk_w,
+                         int32_t* routed_counts, float* P, int32_t* kept_counts,
+                         int32_t* offsets, int32_t* dest_row, uint32_t* dev_status, void* ws,
+                         size_t ws_bytes, void* stream, void* const* events) {
+  return layer_fwd(s, x, gate, gate_bias, W1, W2, y, aux, topk_idx, topk_w, routed_counts, P,
+                   kept_counts, offsets, dest_row, dev_status, ws, ws_bytes, stream, events,
+                   Noise{nullptr, 1.0f});
+}
+
+static moe_status check_noise(const float* noise_u, float temperature) {
+  if (noise_u == nullptr) return MOE_ERR_NULL;
+  if (!aligned16(noise_u)) return MOE_ERR_ALIGN;
+  if (!isfinite(temperature) || !(temperature > 0.0f)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+moe_status moe_route_gumbel(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                            const float* gate_bias, const float* noise_u, float temperature,
+                            int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                            float* aux, float* scores_out, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(check_noise(noise_u, temperature));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(gate);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(topk_w);
+  MOE_OPTIONAL(gate_bias);
+  MOE_OPTIONAL(routed_counts);
+  MOE_OPTIONAL(P);
+  MOE_OPTIONAL(aux);
+  MOE_OPTIONAL(scores_out);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteOut o{topk_idx, topk_w, routed_counts ? routed_counts : w.routed, P ? P : w.P, aux,
+             scores_out};
+  uint32_t* status = dev_status ? dev_status : w.status;
+  MOE_TRY(run_route(d, x, gate, gate_bias, nullptr, o, status, w, st, Noise{noise_u, temperature}));
+  if (d.T > 0) MOE_TRY(run_scan(d, true, o.routed, o.P, aux, nullptr, nullptr, w, st));
+  return MOE_OK;
+}
+
+moe_status moe_layer_fwd_gumbel(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                                const float* gate_bias, const float* noise_u, float temperature,
+                                const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y, float* aux,
+                                int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                                int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events) {
+  MOE_TRY(check_noise(noise_u, temperature));
+  return layer_fwd(s, x, gate, gate_bias, W1, W2, y, aux, topk_idx, topk_w, routed_counts, P,
+                   kept_counts, offsets, dest_row, dev_status, ws, ws_bytes, stream, events,
+                   Noise{noise_u, temperature});
 }
 
 moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes) {

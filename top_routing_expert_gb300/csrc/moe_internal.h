@@ -21,6 +21,8 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;      // waits for in-flight cop
 struct RouteArgs {
   int T, H, E, E_pad, k, n_tiles, stages;
   const float* bias;       // [E] or nullptr (GEMM path only)
+  const float* noise_u;    // [T,E] uniforms in [0,1) for Gumbel noise, or nullptr
+  float temperature;       // scores = (logits + gumbel(u)) / temperature when noise_u
   const float* logits_in;  // [T,E] (logits path only)
   int32_t* topk_idx;       // [T,k]
   float* topk_w;           // [T,k]

@@ -97,18 +97,37 @@ __device__ __forceinline__ void tile_ranks(uint32_t* masks, int E_stride, int E,
 // time in loops that are not unrolled, which keeps the code small.
 constexpr int kChunk = 8;
 
-// Logits of the thread's row from TMEM (GEMM path), plus the bias.
+// Router scores of the thread's row from TMEM (GEMM path): the logits plus
+// the bias, and for the training router (module notes, section 3.1) plus
+// Gumbel noise g = -log(-log(u + 1e-9) + 1e-9) from caller-drawn uniforms,
+// divided by the temperature.
 struct TmemSource {
   uint32_t taddr;       // TMEM address of (this warp's lane quadrant, column 0)
   const float* bias_s;  // shared, zero past E
+  const float* u_row;   // this token's uniforms [E], or nullptr (no noise)
+  float temperature;
+  int E;
   __device__ __forceinline__ void load(int c, float (&v)[kChunk]) const {
     uint32_t r[kChunk];
     tmem_ld_32x32b_x8(taddr + static_cast<uint32_t>(c), r);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]) + bias_s[c + i];
+    if (u_row != nullptr) {
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        if (c + i < E) {
+          const float g = -logf(-logf(u_row[c + i] + 1e-9f) + 1e-9f);
+          v[i] = (v[i] + g) / temperature;
+        }
+      }
+    }
   }
 };
+
+__device__ __forceinline__ const float* noise_row(const RouteArgs& a, int t) {
+  return (a.noise_u != nullptr && t < a.T) ? a.noise_u + static_cast<size_t>(t) * a.E : nullptr;
+}
 
 // Logits of the thread's row from global memory (logits entry point).
 struct GlobalSource {
@@ -463,7 +482,9 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   const int go = __syncthreads_and(done_ok && *sm.abort_flag == 0u);
   tc_fence_after();
   if (go) {
-    TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s};
+    const int t_row = tile * kTileTokens + 32 * (warp & 3) + lane;
+    TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s,
+                   noise_row(a, t_row), a.temperature, a.E};
     // the pipeline stages are free now: they hold the epilogue scratch
     route_epilogue<KMAX>(src, a, tile, carve_epi(smem, npart, KMAX), sm.masks, sm.red, E32,
                          npart, cpt, CtaGroup{});
@@ -675,7 +696,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
       if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
       TmemSource src{tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * E32),
-                     bias_s};
+                     bias_s, noise_row(a, tile * kTileTokens + 32 * q + lane), a.temperature, a.E};
       route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, L.npart, L.cpt, grp);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
