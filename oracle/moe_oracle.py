@@ -43,6 +43,8 @@ R7  Expert FFN: act = bf16(gelu_tanh(x W1_e)); y_e = bf16(act W2_e), no
 R8  Combine: y[t] = bf16( sum over kept slots, ascending j, of w[t,j] y_e ).
 R11 Training router (Gumbel): z = (logits + g)/tau with g from caller-drawn
     uniforms; top-k on z, weights and balance statistics from softmax(z).
+R12 FP8 path: e4m3 with per-token-row scales for activations and
+    per-output-column scales for weights, formed in fp32 (see the FP8 section).
 
 Parity pins for every function here live in tests/test_oracle_pins.py.
 """
@@ -332,6 +334,81 @@ def token_outputs(x_rows, idx_rows, w_rows, kept_rows, W1, W2) -> np.ndarray:
             sel = np.nonzero((idx_rows[:, j] == e) & kept_rows[:, j])[0]
             if sel.size:
                 ye = expert_mlp(x_rows[sel], W1[int(e)], W2[int(e)])
+                acc[sel] += np.asarray(w_rows)[sel, j][:, None] * ye
+    return bf16_round(acc)
+
+
+# ------------------------------------------------------------------ FP8 ---
+# FP8 dispatch and expert FFN (MoE comm bottleneck, section 5.3: FP8 hidden
+# states halve the dispatch/combine bytes). R12: e4m3 values (4 significant
+# bits, exponent bias 7, largest 448, no infinities) with one fp32 scale per
+# token row for activations and one per output column for weights; scales
+# and the scaled values are formed in fp32 exactly as written below, so the
+# quantised bytes are reproducible bit for bit.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 value (ties to even), saturating at +-448, as float64.
+    Normals keep 4 significant bits; below 2^-6 the spacing stays 2^-9."""
+    v = np.asarray(v, np.float64)
+    m, ex = np.frexp(v)
+    ex = np.maximum(ex, -5)
+    q = np.ldexp(np.rint(np.ldexp(v, 4 - ex)), ex - 4)
+    return np.clip(q, -E4M3_MAX, E4M3_MAX)
+
+
+def quantize_rows_fp8(a: np.ndarray):
+    """Per-row e4m3 quantisation: amax = max|a| over the row, inv =
+    fp32(448) / fp32(amax), q = e4m3(fp32(a) * inv), scale = fp32(amax) /
+    fp32(448) (all products and quotients in fp32); a zero row gives q = 0,
+    scale = 0. Returns (q as float64, scale as float64)."""
+    a32 = np.asarray(a, np.float32)
+    amax = np.abs(a32).max(axis=1) if a32.shape[1] else np.zeros(a32.shape[0], np.float32)
+    amax = amax.astype(np.float32)
+    nz = amax > 0
+    inv = np.zeros_like(amax)
+    inv[nz] = np.float32(E4M3_MAX) / amax[nz]
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    q = e4m3_round((a32 * inv[:, None]).astype(np.float32))
+    return q, scale.astype(np.float64)
+
+
+def quantize_weights_fp8(W: np.ndarray):
+    """One expert's weight [K, N] quantised per output column: returns the
+    transposed e4m3 values [N, K] (each output column a row, contiguous over
+    K) and the fp32 column scales [N]."""
+    return quantize_rows_fp8(np.asarray(W).T)
+
+
+def expert_mlp_fp8(xq: np.ndarray, xs: np.ndarray, w1q, w1s, w2q, w2s) -> np.ndarray:
+    """One expert on e4m3 rows: u = xs * w1s * (xq . w1q^T) (float64),
+    act = bf16(gelu_tanh(u)), act quantised per row, y = bf16(as * w2s *
+    (act_q . w2q^T))."""
+    u = (np.asarray(xq) @ np.asarray(w1q, np.float64).T) * xs[:, None] * np.asarray(w1s)[None, :]
+    act = bf16_round(gelu_tanh(u))
+    aq, as_ = quantize_rows_fp8(act)
+    y = (aq @ np.asarray(w2q, np.float64).T) * as_[:, None] * np.asarray(w2s)[None, :]
+    return bf16_round(y)
+
+
+def token_outputs_fp8(x_rows, idx_rows, w_rows, kept_rows, Q1, Q2) -> np.ndarray:
+    """y for a subset of tokens through the FP8 FFN: each token row is
+    quantised once (the dispatch), then every kept expert runs
+    expert_mlp_fp8; Q1[e] = (w1q, w1s), Q2[e] = (w2q, w2s)."""
+    x_rows = np.asarray(x_rows, np.float64)
+    n, H = x_rows.shape
+    xq, xs = quantize_rows_fp8(x_rows)
+    acc = np.zeros((n, H), dtype=np.float64)
+    idx_rows = np.asarray(idx_rows)
+    for e in np.unique(idx_rows):
+        for j in range(idx_rows.shape[1]):
+            sel = np.nonzero((idx_rows[:, j] == e) & kept_rows[:, j])[0]
+            if sel.size:
+                w1q, w1s = Q1[int(e)]
+                w2q, w2s = Q2[int(e)]
+                ye = expert_mlp_fp8(xq[sel], xs[sel], w1q, w1s, w2q, w2s)
                 acc[sel] += np.asarray(w_rows)[sel, j][:, None] * ye
     return bf16_round(acc)
 

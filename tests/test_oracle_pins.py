@@ -453,3 +453,65 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_dispatch_hand_example()
     monkeypatch.undo()
+
+
+# ------------------------------------------------------------------ FP8 ----
+
+def test_e4m3_round_matches_torch():
+    vals = np.concatenate([rng.standard_normal(20000) * 30, rng.standard_normal(2000) * 1e-2,
+                           [0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -6, 1.0, 1.0625, 1.1875, 240.0,
+                            2.0 ** -10, 3 * 2.0 ** -11]]).astype(np.float32)
+    vals = vals[np.abs(vals) <= 448]
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(vals.astype(np.float64)), ref)
+
+
+def test_e4m3_round_hand_cases():
+    cases = {1.0 + 2 ** -4: 1.0, 1.0 + 3 * 2 ** -4: 1.25, 1.0 + 2 ** -4 + 2 ** -20: 1.125,
+             2.0 ** -10: 0.0, 3 * 2.0 ** -11: 2.0 ** -9, 460.0: 448.0, 1e6: 448.0, -1e6: -448.0}
+    for v, want in cases.items():
+        assert O.e4m3_round(np.array([v]))[0] == want, (v, want)
+
+
+def test_row_quantisation_bounds():
+    a = (rng.standard_normal((64, 300)) * np.exp(rng.standard_normal((64, 1)) * 3)).astype(np.float32)
+    a[5] = 0.0
+    q, s = O.quantize_rows_fp8(a)
+    deq = q * s[:, None]
+    # the row maximum lands on +-448 and every element within half a step
+    nz = np.abs(a).max(axis=1) > 0
+    assert np.allclose(np.abs(q[nz]).max(axis=1), 448.0)
+    tiny = np.abs(a) * (448.0 / np.maximum(np.abs(a).max(axis=1, keepdims=True), 1e-30)) < 2 ** -6
+    rel = np.abs(deq - a) / np.maximum(np.abs(a), 1e-30)
+    assert (rel[~tiny & nz[:, None] & (a != 0)] <= 2.0 ** -4 * 1.0001).all()
+    assert (q[5] == 0).all() and s[5] == 0
+
+
+def test_fp8_ffn_is_exact_on_representable_inputs():
+    # inputs already on the e4m3 grid with amax 448 per row/column: scale 1,
+    # so the FP8 FFN's GEMM1 equals the float64 GEMM exactly
+    H, h, n = 64, 96, 20
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 448.0])
+    x = rng.choice(grid, size=(n, H)) * rng.choice([-1, 1], size=(n, H))
+    x[:, 0] = 448.0
+    W1 = rng.choice(grid, size=(H, h)) * rng.choice([-1, 1], size=(H, h))
+    W1[0, :] = 448.0
+    xq, xs = O.quantize_rows_fp8(x)
+    w1q, w1s = O.quantize_weights_fp8(W1)
+    assert np.array_equal(xq, x) and (xs == 1.0).all()
+    assert np.array_equal(w1q, W1.T) and (w1s == 1.0).all()
+    u = (xq @ w1q.T) * xs[:, None] * w1s[None, :]
+    assert np.array_equal(u, x @ W1)
+
+
+def test_fp8_ffn_close_to_bf16_ffn():
+    H, h, n = 256, 384, 200
+    x = O.bf16_round(rng.standard_normal((n, H)))
+    W1 = O.bf16_round(rng.standard_normal((H, h)) / 16)
+    W2 = O.bf16_round(rng.standard_normal((h, H)) / 20)
+    y16 = O.expert_mlp(x, W1, W2)
+    xq, xs = O.quantize_rows_fp8(x)
+    y8 = O.expert_mlp_fp8(xq, xs, *O.quantize_weights_fp8(W1), *O.quantize_weights_fp8(W2))
+    # e4m3 keeps 4 significant bits: a few percent, well away from bf16 error
+    rel = np.abs(y8 - y16).sum() / np.abs(y16).sum()
+    assert 0.005 < rel < 0.08
