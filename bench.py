@@ -132,7 +132,7 @@ def run_ours(args, rank, world, local_rank):
     w = W.get(args.workload)
     inp = W.make_inputs(w, seed=rank)
     s = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
-    ws = moe.Workspace(s, device=dev)
+    ws = moe.Workspace(s, device=dev, fp8=args.fp8)
     d = {kk: (v.to(dev) if v is not None else None) for kk, v in inp.items()}
     T, E, k = w.T, w.E, w.k
     y = torch.empty((T, w.H), dtype=torch.bfloat16, device=dev)
@@ -142,7 +142,16 @@ def run_ours(args, rank, world, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    if args.gumbel is None:
+    if args.fp8:
+        # weights are parameters: quantised once, before the timed region
+        q = moe.Fp8Weights(d["W1"], d["W2"])
+        torch.cuda.synchronize(dev)
+
+        def step(events=None):
+            moe.moe_layer_fwd_fp8(s, d["x"], d["gate"], d["bias"], q, y, aux=aux,
+                                  offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
+                                  stream=stream, events=events)
+    elif args.gumbel is None:
         def step(events=None):
             moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux,
                               offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
@@ -205,7 +214,7 @@ def run_ours(args, rank, world, local_rank):
     any_kept = int((dest >= 0).any(dim=1).sum().item())
 
     # the end-to-end leg times the inference layer; skipped for the training router
-    e2e = None if (args.no_e2e or args.gumbel is not None) else \
+    e2e = None if (args.no_e2e or args.gumbel is not None or args.fp8) else \
         run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
     if rank != 0:
         return None
@@ -274,35 +283,47 @@ def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2
     # the GEMM runs inside a ~1 s loop of back-to-back layer steps under the
     # power cap: the sustained bf16 figure is its roofline (burst also given)
     peak = pk["bf16_tflops_sustained"] or pk["bf16_tflops"]
+    burst = pk["bf16_tflops"]
+    kind = f"{pk['source']} bf16 sustained"
+    if args.fp8:
+        # e4m3 runs at twice the bf16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s dense)
+        peak, burst = 2 * peak, 2 * burst
+        kind = f"{pk['source']} bf16 sustained x 2 (nominal e4m3/bf16 ratio)"
+        for nm in ("gemm1", "gemm2"):
+            kern[nm]["frac_of_measured_fp8"] = round(kern[nm]["frac_of_measured_bf16"] / 2, 3)
+        kern["gemm1"]["includes"] = "GEMM1 + act row quantisation"
     roofline = {"kernel": "grouped GEMM (expert FFN GEMM1+GELU and GEMM2 launches)",
                 "bound": "tensor", "achieved": round(gemm_tf, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(gemm_tf / peak, 4),
-                "peak_kind": f"{pk['source']} bf16 sustained",
-                "frac_of_burst": round(gemm_tf / pk["bf16_tflops"], 4),
-                "traffic": TRAFFIC.get(w.name)}
+                "peak_kind": kind,
+                "frac_of_burst": round(gemm_tf / burst, 4),
+                "traffic": None if args.fp8 else TRAFFIC.get(w.name)}
     tokens = T * world
     line = {
         "metric": METRIC, "value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if args.fp8 else "bf16",
+        "data": "synthetic",
         "config": {**w.describe(), "parallelism": f"replicas x{world} (no exchange)",
                    "router": "inference (top-k of logits)" if args.gumbel is None
                    else f"training (Gumbel noise, temperature {args.gumbel})",
+                   "expert_ffn": "FP8 e4m3 dispatch + FFN, per-row/per-column fp32 scales"
+                   if args.fp8 else "bf16",
                    "l2": l2},
         "clocks": clk,
         "e2e": None if e2e is None else {
             "value": round(tokens / (e2e["ms"] / 1e3), 1), "unit": "tokens/s",
             "ms_per_step": round(e2e["ms"], 4), "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"]},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": (8 if args.fp8 else 7) * args.steps,
         "roofline": roofline,
         "kernels": kern,
         "routing": {"kept_rows": n_kept, "assignments": T * k, "dropped": T * k - n_kept,
                     "dev_status": st},
     }
     if not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(OracleInputs(w, inp), args.cpu_tokens)
+        line["cpu_baseline"] = cpu_baseline(OracleInputs(w, inp, fp8=args.fp8), args.cpu_tokens)
     return line
 
 
@@ -312,15 +333,22 @@ class OracleInputs:
     """Float64 copies of a workload's inputs for the oracle, made once
     (outside any timed region): the oracle works on float64 arrays."""
 
-    def __init__(self, w: W.Workload, inp: dict):
+    def __init__(self, w: W.Workload, inp: dict, fp8: bool = False):
         import numpy as np
+        from oracle import moe_oracle as O
         f64 = lambda t: t.float().numpy().astype(np.float64)
         self.w = w
         self.x = inp["x"]
         self.gate = f64(inp["gate"])
         self.bias = None if inp["bias"] is None else inp["bias"].numpy()
-        self.W1 = [f64(inp["W1"][e]) for e in range(w.E)]
-        self.W2 = [f64(inp["W2"][e]) for e in range(w.E)]
+        self.fp8 = fp8
+        if fp8:
+            # weights quantised once, as the GPU arm does before timing
+            self.Q1 = [O.quantize_weights_fp8(f64(inp["W1"][e])) for e in range(w.E)]
+            self.Q2 = [O.quantize_weights_fp8(f64(inp["W2"][e])) for e in range(w.E)]
+        else:
+            self.W1 = [f64(inp["W1"][e]) for e in range(w.E)]
+            self.W2 = [f64(inp["W2"][e]) for e in range(w.E)]
         self._f64 = f64
 
 
@@ -333,11 +361,17 @@ def cpu_baseline(oi: OracleInputs, n_tokens: int) -> dict:
     n = min(n_tokens, w.T)
     x = oi._f64(oi.x[:n])
     t0 = time.perf_counter()
-    O.layer_forward(x, oi.gate, oi.bias, oi.W1, oi.W2, w.k, w.cf)
+    if oi.fp8:
+        r = O.route_from_logits(O.router_logits(x, oi.gate, oi.bias), w.k)
+        d = O.dispatch_plan(r.idx, w.E, O.capacity(n, w.E, w.k, w.cf))
+        O.token_outputs_fp8(x, r.idx, r.w, d.dest_row >= 0, oi.Q1, oi.Q2)
+    else:
+        O.layer_forward(x, oi.gate, oi.bias, oi.W1, oi.W2, w.k, w.cf)
     dt = time.perf_counter() - t0
     return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"one oracle layer forward of the first {n} of {w.T} tokens "
+            "sample": f"one oracle layer forward{' (FP8 path)' if oi.fp8 else ''} of the "
+                      f"first {n} of {w.T} tokens "
                       f"(float64 numpy, capacity from the sample's own T)"}
 
 
@@ -381,9 +415,13 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 (e4m3) dispatch and expert FFN (weights quantised before timing)")
     ap.add_argument("--gumbel", type=float, default=None, metavar="TAU",
                     help="time the layer with the Gumbel training router at temperature TAU")
     args = ap.parse_args()
+    if args.fp8 and args.gumbel is not None:
+        ap.error("--fp8 and --gumbel are separate benchmark lines")
     if args.warmup < 3:
         args.warmup = 3
 

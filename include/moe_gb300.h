@@ -239,6 +239,63 @@ MOE_API moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const
                               uint32_t* dev_status, void* ws, size_t ws_bytes,
                               void* const* streams, void* const* events);
 
+/* ------------------------------------------------------------- FP8 ----
+ * FP8 (e4m3) dispatch and expert FFN: the MoE comm bottleneck page, section
+ * 5.3, sends FP8 hidden states to halve the dispatch bytes; here the
+ * dispatched rows are e4m3 and both expert GEMMs run on the FP8 tensor-core
+ * path. Scaling (one reading; the page fixes none): one fp32 scale per row
+ * of activations and per output column of weights. For a row with largest
+ * magnitude amax: inv = 448 / amax, q = e4m3(v * inv) (round to nearest
+ * even, saturating at +-448), scale = amax / 448, all in fp32; a zero row
+ * has q = 0 and scale = 0. A GEMM of quantised operands is the fp32 sum of
+ * q products times the row scale times the column scale. e4m3 arrays hold
+ * raw bytes. */
+
+/* Bytes of device workspace the FP8 entry points need (more than
+ * moe_workspace_size: row scales and the quantised activations). Host only. */
+MOE_API moe_status moe_workspace_size_fp8(const moe_shape* s, size_t* bytes);
+
+/* Weight quantisation, done once per weight tensor: W [E,K,N] bf16 (K the
+ * input dimension) -> Wq [E,N,K] e4m3, each output column a contiguous row,
+ * and w_scale [E,N] fp32 column scales. For the layer: W1 gives W1q [E,h,H]
+ * and w1_scale [E,h]; W2 gives W2q [E,H,h] and w2_scale [E,H].
+ * 1 <= E <= 256; K, N multiples of 64, at most 65536. Needs no workspace
+ * (w_scale doubles as scratch). */
+MOE_API moe_status moe_quantize_weights_fp8(int64_t E, int64_t K, int64_t N, const moe_bf16* W,
+                                    uint8_t* Wq, float* w_scale, void* stream);
+
+/* moe_permute with an FP8 payload: each token row is quantised once with
+ * its own scale, and the e4m3 row and scale go to every kept destination:
+ * x_q [T*k,H] e4m3 and x_scale [T*k] fp32 instead of x_perm. Other
+ * arguments, results and the workspace as moe_permute. */
+MOE_API moe_status moe_permute_fp8(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+                           int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                           int32_t* src_token, uint8_t* x_q, float* x_scale,
+                           uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_expert_ffn on e4m3 rows: u = x_scale[r] * w1_scale[e,:] * (x_q[r] .
+ * W1q[e]^T) in fp32; act [T*k,h] bf16 = bf16(gelu_tanh(u)); act is
+ * quantised per row (scale from the largest |act| of the row) and
+ * y_perm [T*k,H] bf16 = bf16(act_scale[r] * w2_scale[e,:] * (act_q[r] .
+ * W2q[e]^T)). ws must hold moe_workspace_size_fp8 bytes. */
+MOE_API moe_status moe_expert_ffn_fp8(const moe_shape* s, const uint8_t* x_q, const float* x_scale,
+                              const int32_t* offsets, const uint8_t* W1q, const float* w1_scale,
+                              const uint8_t* W2q, const float* w2_scale, moe_bf16* act,
+                              moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* moe_layer_fwd with the FP8 dispatch and FP8 expert FFN (weights from
+ * moe_quantize_weights_fp8); the router and the combine are those of
+ * moe_layer_fwd. ws must hold moe_workspace_size_fp8 bytes. events as in
+ * moe_layer_fwd, events[4] recorded after GEMM1 and the act quantisation. */
+MOE_API moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                             const float* gate_bias, const uint8_t* W1q, const float* w1_scale,
+                             const uint8_t* W2q, const float* w2_scale, moe_bf16* y, float* aux,
+                             int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                             int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                             uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
+                             void* const* events);
+
 /* moe_permute for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it serves code that may not call
  * cudaMalloc or hold a workspace: a plugin inside a runtime that owns all

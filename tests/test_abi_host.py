@@ -177,3 +177,30 @@ def test_status_strings(lib):
     for code in range(7):
         assert moe.status_str(code)
     assert moe.status_str(0) == "ok"
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    s = _shape()
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    n8 = ctypes.c_size_t()
+    assert lib.moe_workspace_size_fp8(ctypes.byref(s), ctypes.byref(n8)) == 0
+    n = _status(lib, s)[1]
+    A = 64 * 2
+    # row scales, e4m3 act and its row maxima on top of the bf16 layer's scratch
+    assert n8.value >= n + A * 128 + 3 * A * 4
+    assert lib.moe_workspace_size_fp8(ctypes.byref(_shape(h=96)), ctypes.byref(n8)) == 3
+    # weight quantisation: shape, NULL and alignment checks
+    assert lib.moe_quantize_weights_fp8(0, 128, 128, f, f, f, None) == 2
+    assert lib.moe_quantize_weights_fp8(8, 96, 128, f, f, f, None) == 3
+    assert lib.moe_quantize_weights_fp8(8, 128, 128, None, f, f, None) == 1
+    assert lib.moe_quantize_weights_fp8(8, 128, 128, f, P(FAKE + 4), f, None) == 5
+    # the FP8 layer needs the FP8 workspace size
+    assert lib.moe_layer_fwd_fp8(ctypes.byref(s), f, f, None, f, f, f, f, f, *[None] * 9,
+                                 f, n, None, None) == 4
+    assert lib.moe_layer_fwd_fp8(ctypes.byref(s), f, f, None, f, None, f, f, f, *[None] * 9,
+                                 f, n8.value, None, None) == 1
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, None, f, f, f, f, f, f, f, None, f,
+                                  n8.value, None) == 1
+    assert lib.moe_permute_fp8(ctypes.byref(s), f, f, None, f, f, None, f, None, None, f, n,
+                               None) == 1

@@ -22,6 +22,8 @@ __all__ = [
     "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
     "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
+    "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
+    "moe_layer_fwd_fp8", "Fp8Weights",
     "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
@@ -32,7 +34,8 @@ EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "mo
                     "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
                     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc",
                     "moe_host_workspace_size", "moe_layer_fwd_host", "moe_route_gumbel",
-                    "moe_layer_fwd_gumbel"]
+                    "moe_layer_fwd_gumbel", "moe_workspace_size_fp8", "moe_quantize_weights_fp8",
+                    "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8"]
 
 
 class MoeError(RuntimeError):
@@ -94,6 +97,16 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_host_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_layer_fwd_host.restype = ctypes.c_int
     lib.moe_layer_fwd_host.argtypes = [S, ctypes.c_int64] + [_P] * 9 + [ctypes.c_size_t, _P, _P]
+    lib.moe_workspace_size_fp8.restype = ctypes.c_int
+    lib.moe_workspace_size_fp8.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_quantize_weights_fp8.restype = ctypes.c_int
+    lib.moe_quantize_weights_fp8.argtypes = [ctypes.c_int64] * 3 + [_P] * 4
+    lib.moe_permute_fp8.restype = ctypes.c_int
+    lib.moe_permute_fp8.argtypes = [S] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.moe_expert_ffn_fp8.restype = ctypes.c_int
+    lib.moe_expert_ffn_fp8.argtypes = [S] + [_P] * 11 + [ctypes.c_size_t, _P]
+    lib.moe_layer_fwd_fp8.restype = ctypes.c_int
+    lib.moe_layer_fwd_fp8.argtypes = [S] + [_P] * 18 + [ctypes.c_size_t, _P, _P]
     _lib = lib
     return lib
 
@@ -151,12 +164,20 @@ def workspace_size(shape) -> int:
     return n.value
 
 
-class Workspace:
-    """Caller-owned device scratch for one shape (a torch uint8 tensor)."""
+def workspace_size_fp8(shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size_fp8",
+           load_library().moe_workspace_size_fp8(ctypes.byref(_shape(shape)), ctypes.byref(n)))
+    return n.value
 
-    def __init__(self, shape, device="cuda"):
+
+class Workspace:
+    """Caller-owned device scratch for one shape (a torch uint8 tensor);
+    fp8=True sizes it for the FP8 entry points too."""
+
+    def __init__(self, shape, device="cuda", fp8: bool = False):
         self.shape = _shape(shape)
-        self.nbytes = workspace_size(self.shape)
+        self.nbytes = workspace_size_fp8(self.shape) if fp8 else workspace_size(self.shape)
         self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
 
     @property
@@ -364,3 +385,79 @@ def moe_layer_fwd_gumbel(shape, x, gate, gate_bias, noise_u, temperature, W1, W2
         _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
         _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
+
+
+# --------------------------------------------------------------- FP8 ----
+
+def moe_quantize_weights_fp8(W, Wq, w_scale, stream=None):
+    """W [E,K,N] bf16 -> Wq [E,N,K] e4m3 bytes (uint8) and w_scale [E,N] fp32."""
+    if W.dim() != 3:
+        raise ValueError("W must be [E, K, N]")
+    E, K, N = W.shape
+    _check("moe_quantize_weights_fp8", load_library().moe_quantize_weights_fp8(
+        E, K, N, _ptr(W, torch.bfloat16, "W"), _ptr(Wq, torch.uint8, "Wq"),
+        _ptr(w_scale, torch.float32, "w_scale"), _stream(stream)))
+
+
+class Fp8Weights:
+    """The expert weights quantised for the FP8 layer: W1q [E,h,H], W2q
+    [E,H,h] (e4m3 bytes, each output column a row) and their column scales
+    w1_scale [E,h], w2_scale [E,H]."""
+
+    def __init__(self, W1, W2, stream=None):
+        E, H, h = W1.shape
+        dev = W1.device
+        self.W1q = torch.empty((E, h, H), dtype=torch.uint8, device=dev)
+        self.w1_scale = torch.empty((E, h), dtype=torch.float32, device=dev)
+        self.W2q = torch.empty((E, H, h), dtype=torch.uint8, device=dev)
+        self.w2_scale = torch.empty((E, H), dtype=torch.float32, device=dev)
+        moe_quantize_weights_fp8(W1, self.W1q, self.w1_scale, stream)
+        moe_quantize_weights_fp8(W2, self.W2q, self.w2_scale, stream)
+
+
+def moe_permute_fp8(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x_q, x_scale,
+                    dev_status=None, ws: Workspace | None = None, stream=None):
+    """moe_permute with an e4m3 payload: x_q [T*k,H] uint8, x_scale [T*k] fp32."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_permute_fp8", load_library().moe_permute_fp8(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
+        _ptr(x_q, torch.uint8, "x_q"), _ptr(x_scale, torch.float32, "x_scale"),
+        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+
+
+def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm,
+                       dev_status=None, ws: Workspace | None = None, stream=None):
+    """Expert FFN on e4m3 rows; ws must be an fp8=True workspace."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_expert_ffn_fp8", load_library().moe_expert_ffn_fp8(
+        ctypes.byref(s), _ptr(x_q, torch.uint8, "x_q"), _ptr(x_scale, torch.float32, "x_scale"),
+        _ptr(offsets, torch.int32, "offsets"), _ptr(q.W1q, torch.uint8, "W1q"),
+        _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
+        _ptr(q.w2_scale, torch.float32, "w2_scale"), _ptr(act, torch.bfloat16, "act"),
+        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
+
+
+def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, topk_idx=None,
+                      topk_w=None, routed_counts=None, P=None, kept_counts=None, offsets=None,
+                      dest_row=None, dev_status=None, ws: Workspace | None = None, stream=None,
+                      events=None):
+    """moe_layer_fwd with the FP8 dispatch and expert FFN; ws must be an
+    fp8=True workspace."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    ev = _events(events)
+    _check("moe_layer_fwd_fp8", load_library().moe_layer_fwd_fp8(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(q.W1q, torch.uint8, "W1q"),
+        _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
+        _ptr(q.w2_scale, torch.float32, "w2_scale"), _ptr(y, torch.bfloat16, "y"),
+        _ptr(aux, torch.float32, "aux"), _ptr(topk_idx, torch.int32, "topk_idx"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
+        _ptr(P, torch.float32, "P"), _ptr(kept_counts, torch.int32, "kept_counts"),
+        _ptr(offsets, torch.int32, "offsets"), _ptr(dest_row, torch.int32, "dest_row"),
+        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))

@@ -47,6 +47,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
     if ((x) != cudaSuccess) return MOE_ERR_CUDA;   \
   } while (0)
 
+#define MOE_TRY(x)                         \
+  do {                                     \
+    const moe_status _s = (x);             \
+    if (_s != MOE_OK) return _s;           \
+  } while (0)
+
 // ------------------------------------------------------------- workspace ----
 
 struct Ws {
@@ -69,6 +75,12 @@ struct Ws {
   uint16_t* x_perm;
   uint16_t* act;
   uint16_t* y_perm;
+  // FP8 path only (moe_workspace_size_fp8); the e4m3 dispatched rows live in
+  // the x_perm bytes
+  float* x_scale;
+  uint8_t* act_q;
+  float* act_scale;
+  uint32_t* act_amax;
 };
 
 struct Dims {
@@ -92,7 +104,7 @@ Dims dims_of(const moe_shape* s) {
 
 // Lays the scratch arrays out from `base` (256-byte aligned pieces); with
 // base == nullptr only the size is computed.
-size_t layout(const Dims& d, uint8_t* base, Ws* w) {
+size_t layout(const Dims& d, uint8_t* base, Ws* w, bool fp8 = false) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> void* {
     void* p = base ? base + off : nullptr;
@@ -121,16 +133,27 @@ size_t layout(const Dims& d, uint8_t* base, Ws* w) {
   v.x_perm = static_cast<uint16_t*>(take(A * d.H * 2));
   v.act = static_cast<uint16_t*>(take(A * d.h * 2));
   v.y_perm = static_cast<uint16_t*>(take(A * d.H * 2));
+  v.x_scale = nullptr;
+  v.act_q = nullptr;
+  v.act_scale = nullptr;
+  v.act_amax = nullptr;
+  if (fp8) {
+    v.x_scale = static_cast<float*>(take(A * 4));
+    v.act_q = static_cast<uint8_t*>(take(A * d.h));
+    v.act_scale = static_cast<float*>(take(A * 4));
+    v.act_amax = static_cast<uint32_t*>(take(A * 4));
+  }
   if (w) *w = v;
   return off;
 }
 
-moe_status carve(const moe_shape* s, const Dims& d, void* ws, size_t ws_bytes, Ws* w) {
-  const size_t need = layout(d, nullptr, nullptr);
+moe_status carve(const moe_shape* s, const Dims& d, void* ws, size_t ws_bytes, Ws* w,
+                 bool fp8 = false) {
+  const size_t need = layout(d, nullptr, nullptr, fp8);
   if (ws == nullptr) return MOE_ERR_NULL;
   if (!aligned16(ws)) return MOE_ERR_ALIGN;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
-  layout(d, static_cast<uint8_t*>(ws), w);
+  layout(d, static_cast<uint8_t*>(ws), w, fp8);
   (void)s;
   return MOE_OK;
 }
@@ -199,6 +222,20 @@ bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
   const cuuint32_t estride[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A byte (e4m3) row-major matrix [outer, inner] in 128 x 128 boxes (one
+// 128-byte swizzle row of K per box row); inner must be a multiple of 16.
+bool tmap_u8_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t gdim[2] = {inner, outer};
+  const cuuint64_t gstride[1] = {inner};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -307,6 +344,29 @@ moe_status run_gather(const Dims& d, const moe_bf16* x, const int32_t* idx, cons
   return MOE_OK;
 }
 
+moe_status run_gather_fp8(const Dims& d, const moe_bf16* x, const int32_t* idx,
+                          const int32_t* offsets, int32_t* dest_row, int32_t* src_token,
+                          uint8_t* xq, float* xs, uint32_t* status, const Ws& w, cudaStream_t st) {
+  GatherArgs g;
+  g.T = d.T;
+  g.H = d.H;
+  g.E = d.E;
+  g.k = d.k;
+  g.n_tiles = d.n_tiles;
+  g.C = d.C;
+  g.x = x;
+  g.topk_idx = idx;
+  g.rank8 = w.rank8;
+  g.tile_base = w.tile_base;
+  g.offsets = offsets;
+  g.dest_row = dest_row;
+  g.src_token = src_token;
+  g.x_perm = nullptr;
+  g.dev_status = status;
+  MOE_CUDA(launch_gather_fp8(g, xq, xs, num_sms(), st));
+  return MOE_OK;
+}
+
 moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const int32_t* offsets,
                     int K, int N, moe_bf16* D, int gelu, uint32_t* status, cudaStream_t st) {
   if (d.A == 0) return MOE_OK;
@@ -321,12 +381,61 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.rows = static_cast<int>(d.A);
   g.D = D;
   g.gelu = gelu;
+  g.a_scale = nullptr;
+  g.b_scale = nullptr;
+  g.row_amax = nullptr;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   if (d.A >= kPairGemmMinRows)
     MOE_CUDA(launch_grouped_gemm_pair(tm_a, tm_b, g, num_sms(), st));
   else
     MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));
+  return MOE_OK;
+}
+
+// The FP8 grouped GEMM (CTA-pair kernel at every size): A e4m3 [A, K] with
+// row scales, B^T e4m3 [E*N, K] with column scales; with row_amax the
+// epilogue also records each output row's largest magnitude.
+moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
+                        const uint8_t* Wq, const float* w_scale, const int32_t* offsets, int K,
+                        int N, moe_bf16* D, int gelu, uint32_t* row_amax, uint32_t* status,
+                        cudaStream_t st) {
+  if (d.A == 0) return MOE_OK;
+  CUtensorMap tm_a, tm_b;
+  if (!tmap_u8_2d(&tm_a, Aq, K, d.A)) return MOE_ERR_CUDA;
+  if (!tmap_u8_2d(&tm_b, Wq, K, static_cast<uint64_t>(d.E) * N)) return MOE_ERR_CUDA;
+  GemmArgs g;
+  g.offsets = offsets;
+  g.E = d.E;
+  g.K = K;
+  g.N = N;
+  g.rows = static_cast<int>(d.A);
+  g.D = D;
+  g.gelu = gelu;
+  g.a_scale = a_scale;
+  g.b_scale = w_scale;
+  g.row_amax = row_amax;
+  g.dev_status = status;
+  g.timeout_ns = wait_timeout_ns();
+  MOE_CUDA(launch_grouped_gemm_pair_fp8(tm_a, tm_b, g, num_sms(), st));
+  return MOE_OK;
+}
+
+// FP8 expert FFN on dispatched e4m3 rows: GEMM1 (+GELU, row maxima of act),
+// act quantised per row, GEMM2.
+moe_status run_ffn_fp8(const Dims& d, const uint8_t* xq, const float* xs, const int32_t* offsets,
+                       const uint8_t* W1q, const float* w1s, const uint8_t* W2q,
+                       const float* w2s, moe_bf16* act, moe_bf16* y_perm, uint32_t* status,
+                       const Ws& w, cudaStream_t st, void* const* events) {
+  if (d.A == 0) return MOE_OK;
+  MOE_CUDA(cudaMemsetAsync(w.act_amax, 0, sizeof(uint32_t) * static_cast<size_t>(d.A), st));
+  MOE_TRY(run_gemm_fp8(d, xq, xs, W1q, w1s, offsets, d.H, d.h, act, 1, w.act_amax, status, st));
+  MOE_CUDA(launch_row_quant(act, w.act_amax, w.act_q, w.act_scale, offsets, d.E,
+                            static_cast<int>(d.A), d.h, num_sms(), st));
+  if (events && cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  MOE_TRY(run_gemm_fp8(d, w.act_q, w.act_scale, W2q, w2s, offsets, d.h, d.H, y_perm, 0, nullptr,
+                       status, st));
   return MOE_OK;
 }
 
@@ -343,12 +452,6 @@ moe_status run_combine(const Dims& d, const moe_bf16* y_perm, const int32_t* des
   MOE_CUDA(launch_combine(c, num_sms(), st));
   return MOE_OK;
 }
-
-#define MOE_TRY(x)                         \
-  do {                                     \
-    const moe_status _s = (x);             \
-    if (_s != MOE_OK) return _s;           \
-  } while (0)
 
 }  // namespace
 
@@ -511,17 +614,33 @@ moe_status moe_combine(const moe_shape* s, const moe_bf16* y_perm, const int32_t
   return run_combine(d, y_perm, dest_row, topk_w, y, static_cast<cudaStream_t>(stream));
 }
 
+// Quantised expert weights of the FP8 layer: W1q [E,h,H], W2q [E,H,h] e4m3
+// (transposed), w1s [E,h], w2s [E,H] column scales.
+struct Fp8Weights {
+  const uint8_t* W1q;
+  const float* w1s;
+  const uint8_t* W2q;
+  const float* w2s;
+};
+
 static moe_status layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
                      const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y,
                      float* aux, int32_t* topk_idx, float* topk_w, int32_t* routed_counts,
                      float* P, int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
                      uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
-                     void* const* events, Noise noise) {
+                     void* const* events, Noise noise, const Fp8Weights* q = nullptr) {
   MOE_TRY(check_shape(s));
   MOE_REQUIRE(x);
   MOE_REQUIRE(gate);
-  MOE_REQUIRE(W1);
-  MOE_REQUIRE(W2);
+  if (q == nullptr) {
+    MOE_REQUIRE(W1);
+    MOE_REQUIRE(W2);
+  } else {
+    MOE_REQUIRE(q->W1q);
+    MOE_REQUIRE(q->w1s);
+    MOE_REQUIRE(q->W2q);
+    MOE_REQUIRE(q->w2s);
+  }
   MOE_REQUIRE(y);
   MOE_OPTIONAL(gate_bias);
   MOE_OPTIONAL(aux);
@@ -535,7 +654,7 @@ static moe_status layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf1
   MOE_OPTIONAL(dev_status);
   const Dims d = dims_of(s);
   Ws w;
-  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w, q != nullptr));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = dev_status ? dev_status : w.status;
   int32_t* idx = topk_idx ? topk_idx : w.topk_idx;
@@ -565,11 +684,19 @@ static moe_status layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf1
   if (!mark(1)) return MOE_ERR_CUDA;
   MOE_TRY(run_scan(d, true, routed, Pp, aux, kept, off, w, st));
   if (!mark(2)) return MOE_ERR_CUDA;
-  MOE_TRY(run_gather(d, x, idx, off, dest, w.src_token, w.x_perm, status, w, st));
-  if (!mark(3)) return MOE_ERR_CUDA;
-  MOE_TRY(run_gemm(d, w.x_perm, W1, off, d.H, d.h, w.act, 1, status, st));
-  if (!mark(4)) return MOE_ERR_CUDA;
-  MOE_TRY(run_gemm(d, w.act, W2, off, d.h, d.H, w.y_perm, 0, status, st));
+  if (q == nullptr) {
+    MOE_TRY(run_gather(d, x, idx, off, dest, w.src_token, w.x_perm, status, w, st));
+    if (!mark(3)) return MOE_ERR_CUDA;
+    MOE_TRY(run_gemm(d, w.x_perm, W1, off, d.H, d.h, w.act, 1, status, st));
+    if (!mark(4)) return MOE_ERR_CUDA;
+    MOE_TRY(run_gemm(d, w.act, W2, off, d.h, d.H, w.y_perm, 0, status, st));
+  } else {
+    uint8_t* xq = reinterpret_cast<uint8_t*>(w.x_perm);
+    MOE_TRY(run_gather_fp8(d, x, idx, off, dest, w.src_token, xq, w.x_scale, status, w, st));
+    if (!mark(3)) return MOE_ERR_CUDA;
+    MOE_TRY(run_ffn_fp8(d, xq, w.x_scale, off, q->W1q, q->w1s, q->W2q, q->w2s, w.act, w.y_perm,
+                        status, w, st, events ? events + 4 : nullptr));
+  }
   if (!mark(5)) return MOE_ERR_CUDA;
   MOE_TRY(run_combine(d, w.y_perm, dest, wts, y, st));
   if (!mark(6)) return MOE_ERR_CUDA;
@@ -634,6 +761,104 @@ moe_status moe_layer_fwd_gumbel(const moe_shape* s, const moe_bf16* x, const moe
   return layer_fwd(s, x, gate, gate_bias, W1, W2, y, aux, topk_idx, topk_w, routed_counts, P,
                    kept_counts, offsets, dest_row, dev_status, ws, ws_bytes, stream, events,
                    Noise{noise_u, temperature});
+}
+
+moe_status moe_workspace_size_fp8(const moe_shape* s, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_NULL;
+  MOE_TRY(check_shape(s));
+  *bytes = layout(dims_of(s), nullptr, nullptr, true);
+  return MOE_OK;
+}
+
+moe_status moe_quantize_weights_fp8(int64_t E, int64_t K, int64_t N, const moe_bf16* W,
+                                    uint8_t* Wq, float* w_scale, void* stream) {
+  if (E <= 0 || K <= 0 || N <= 0) return MOE_ERR_SHAPE;
+  if (E > kMaxExperts || K % 64 != 0 || N % 64 != 0 || K > kMaxDim || N > kMaxDim)
+    return MOE_ERR_UNSUPPORTED;
+  MOE_REQUIRE(W);
+  MOE_REQUIRE(Wq);
+  MOE_REQUIRE(w_scale);
+  MOE_CUDA(launch_quantize_weights(W, Wq, w_scale, static_cast<int>(E), static_cast<int>(K),
+                                   static_cast<int>(N), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_permute_fp8(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
+                           int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                           int32_t* src_token, uint8_t* x_q, float* x_scale,
+                           uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(dest_row);
+  MOE_REQUIRE(x_q);
+  MOE_REQUIRE(x_scale);
+  MOE_OPTIONAL(kept_counts);
+  MOE_OPTIONAL(src_token);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = dev_status ? dev_status : w.status;
+  if (d.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), st));
+    if (kept_counts) MOE_CUDA(cudaMemsetAsync(kept_counts, 0, sizeof(int32_t) * d.E, st));
+    return MOE_OK;
+  }
+  RankArgs r;
+  r.T = d.T;
+  r.E = d.E;
+  r.k = d.k;
+  r.n_tiles = d.n_tiles;
+  r.topk_idx = topk_idx;
+  r.tile_cnt = w.tile_cnt;
+  r.rank8 = w.rank8;
+  r.ticket = w.ticket;
+  r.dev_status = status;
+  MOE_CUDA(launch_rank(r, st));
+  MOE_TRY(run_scan(d, false, w.routed, w.P, nullptr, kept_counts, offsets, w, st));
+  MOE_TRY(run_gather_fp8(d, x, topk_idx, offsets, dest_row, src_token, x_q, x_scale, status, w,
+                         st));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_fp8(const moe_shape* s, const uint8_t* x_q, const float* x_scale,
+                              const int32_t* offsets, const uint8_t* W1q, const float* w1_scale,
+                              const uint8_t* W2q, const float* w2_scale, moe_bf16* act,
+                              moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                              void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x_q);
+  MOE_REQUIRE(x_scale);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(W1q);
+  MOE_REQUIRE(w1_scale);
+  MOE_REQUIRE(W2q);
+  MOE_REQUIRE(w2_scale);
+  MOE_REQUIRE(act);
+  MOE_REQUIRE(y_perm);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w, true));
+  uint32_t* status = dev_status ? dev_status : w.status;
+  return run_ffn_fp8(d, x_q, x_scale, offsets, W1q, w1_scale, W2q, w2_scale, act, y_perm, status,
+                     w, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
+                             const float* gate_bias, const uint8_t* W1q, const float* w1_scale,
+                             const uint8_t* W2q, const float* w2_scale, moe_bf16* y, float* aux,
+                             int32_t* topk_idx, float* topk_w, int32_t* routed_counts, float* P,
+                             int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                             uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
+                             void* const* events) {
+  const Fp8Weights q{W1q, w1_scale, W2q, w2_scale};
+  return layer_fwd(s, x, gate, gate_bias, nullptr, nullptr, y, aux, topk_idx, topk_w,
+                   routed_counts, P, kept_counts, offsets, dest_row, dev_status, ws, ws_bytes,
+                   stream, events, Noise{nullptr, 1.0f}, &q);
 }
 
 moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes) {

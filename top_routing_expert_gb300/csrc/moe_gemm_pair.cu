@@ -65,9 +65,15 @@ __device__ __forceinline__ float gelu_tanh_f(float u) {
   return __fdividef(u, 1.0f + __expf(-z2));
 }
 
+// kFp8: A and B are e4m3 (both K-major, 128 elements = 128 bytes per
+// stage row), the UMMA is kind::f8f6f4 and the epilogue multiplies by the
+// row scale of A and the column scale of B. Otherwise bf16 A (K-major) and
+// bf16 B (MN-major), 64 elements per stage row.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, GemmArgs p) {
+  constexpr int kKE = kFp8 ? 128 : kBlockK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_pm = pm_prefix[E];
   const int n_tiles_n = (p.N + kBN - 1) / kBN;
   const int total = total_pm * n_tiles_n;
-  const int nk = p.K / kBlockK;
+  const int nk = (p.K + kKE - 1) / kKE;  // a partial last block reads zeros past K
   const WaitCtl wc{abort_flag, p.dev_status, p.timeout_ns};
 
   if (warp == 0) {
@@ -167,11 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
           // A rows are reused by every n-tile of the group: keep them in L2
-          tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kBlockK, c.row0, pol_a);
+          tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
+          if constexpr (kFp8) {
+            // B^T [E*N, K] e4m3: this CTA's 128 output columns as K-major rows
+            tma_load_2d_pair(sb, &tm_b, bar, kb * kKE, c.e * p.N + b_col);
+          } else {
 #pragma unroll
-          for (int cb = 0; cb < kBN / 2 / 64; ++cb)
-            tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
-                             b_row + kb * kBlockK);
+            for (int cb = 0; cb < kBN / 2 / 64; ++cb)
+              tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
+                               b_row + kb * kBlockK);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -205,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------- UMMA issuer (leader) ----
-      const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, false, true);
+      const uint32_t idesc =
+          kFp8 ? idesc_e4m3_f32(2 * kBM, kBN) : idesc_bf16_f32(2 * kBM, kBN, false, true);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -224,13 +236,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            // A: K-major 128-byte rows, 16-element K step = 32 bytes.
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: K-major 128-byte rows; one UMMA K step (16 bf16 or 32 e4m3)
+            // is 32 bytes.
             const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-            // B: MN-major, one 128-byte row per k, 16-row K step = 2 KB,
-            // this CTA's two 64-column blocks 8 KB apart.
-            const uint64_t bd = smem_desc_sw128(b_addr + 2048u * kk, 64u * kBlockK * 2, 1024u);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (kFp8) {
+              // B: K-major like A
+              const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
+              umma_f8_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            } else {
+              // B: MN-major, one 128-byte row per k, 16-row K step = 2 KB,
+              // this CTA's two 64-column blocks 8 KB apart.
+              const uint64_t bd = smem_desc_sw128(b_addr + 2048u * kk, 64u * kBlockK * 2, 1024u);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == kStages) {
@@ -263,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = c.row0 + 32 * q + lane;
       const bool valid = row < c.row_end;
       uint16_t* drow = p.D + static_cast<size_t>(valid ? row : 0) * p.N;
+      float row_max = 0.f;  // FP8 mode: max |output| of this row in this tile
       const uint32_t t_base =
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * kBN);
 #pragma unroll 1
@@ -274,14 +294,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (valid) {
           uint32_t packed[16];
+          float rs = 1.f;
+          const float* cs = nullptr;
+          if constexpr (kFp8) {
+            rs = p.a_scale[row];
+            cs = p.b_scale + static_cast<size_t>(c.e) * p.N + col;
+          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float v0 = __uint_as_float(r[2 * i]);
             float v1 = __uint_as_float(r[2 * i + 1]);
+            if constexpr (kFp8) {
+              v0 = v0 * rs * cs[2 * i];
+              v1 = v1 * rs * cs[2 * i + 1];
+            }
             if (p.gelu) {
               v0 = gelu_tanh_f(v0);
               v1 = gelu_tanh_f(v1);
             }
+            if constexpr (kFp8) row_max = fmaxf(row_max, fmaxf(fabsf(v0), fabsf(v1)));
             packed[i] = pack_bf16x2(v0, v1);
           }
           // outputs are read once, by the next kernel: stream them past L2
@@ -291,6 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
                                                 packed[4 * i + 3]));
         }
+      }
+      if constexpr (kFp8) {
+        // bf16 rounding is monotonic, so the rounded maximum is the maximum
+        // of the rounded (stored) values
+        if (p.row_amax != nullptr && valid && c.n0 < p.N)
+          atomicMax(p.row_amax + row, __float_as_uint(bf16_lo(pack_bf16x2(row_max, 0.f))));
       }
       tc_fence_before();
       mbar_arrive_cluster(tempty_leader[acc]);
@@ -316,10 +353,11 @@ size_t gemm_pair_smem_bytes(int E) {
          8 * static_cast<size_t>(E + 1);
 }
 
-cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                     const GemmArgs& a, int num_sms, cudaStream_t st) {
+template <bool kFp8>
+cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+                        int num_sms, cudaStream_t st) {
   const size_t smem = gemm_pair_smem_bytes(a.E);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel,
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -335,9 +373,19 @@ cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel, tm_a, tm_b, a);
+  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8>, tm_a, tm_b, a);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                     const GemmArgs& a, int num_sms, cudaStream_t st) {
+  return launch_pair<false>(tm_a, tm_b, a, num_sms, st);
+}
+
+cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                         const GemmArgs& a, int num_sms, cudaStream_t st) {
+  return launch_pair<true>(tm_a, tm_b, a, num_sms, st);
 }
 
 }  // namespace moe

@@ -94,6 +94,10 @@ struct GemmArgs {
   int rows;                // rows of the A and D buffers (T*k)
   uint16_t* D;             // [rows, N] bf16
   int gelu;                // 1: act = gelu_tanh(acc), 0: plain
+  const float* a_scale;    // FP8 mode: per-row scales of A [rows]
+  const float* b_scale;    // FP8 mode: per-column scales of B [E, N]
+  uint32_t* row_amax;      // FP8 mode, optional: max |bf16 output| per row, fp32 bits,
+                           // combined with atomicMax (zeroed by the caller)
   uint32_t* dev_status;
   uint64_t timeout_ns;
 };
@@ -117,5 +121,14 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st);
 size_t gemm_pair_smem_bytes(int E);
+cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                         const GemmArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, int E, int K,
+                                    int N, cudaStream_t st);
+cudaError_t launch_row_quant(const uint16_t* src, const uint32_t* amax, uint8_t* dst,
+                             float* scale, const int32_t* offsets, int E, int rows, int K,
+                             int num_sms, cudaStream_t st);
+cudaError_t launch_gather_fp8(const GatherArgs& a, uint8_t* xq, float* xs, int num_sms,
+                              cudaStream_t st);
 
 }  // namespace moe
