@@ -54,18 +54,21 @@ def peaks():
 
 # ------------------------------------------------------------ accounting ----
 
-def algorithmic_work(w: W.Workload, n_kept: int, n_tokens_any: int) -> dict:
+def algorithmic_work(w: W.Workload, n_kept: int, n_tokens_any: int, fp8: bool = False) -> dict:
     """What each stage must move or compute (not what it happens to move):
     router reads x and the gate and writes indices/weights; permute reads
     each token row that has a kept slot once and writes each kept row once
     (dispatch bytes of the comm bottleneck page, section 2.1, with drops
     removed); GEMM1/GEMM2 are 2*N*H*h FLOP each (4*H*h per token-expert,
-    section 2.2); combine reads each kept row and writes each token row."""
+    section 2.2); combine reads each kept row and writes each token row.
+    With FP8 the permute writes e4m3 rows (1 byte per value) and a 4-byte
+    scale per kept row."""
     T, H, E, k, h = w.T, w.H, w.E, w.k, w.h
+    permute = 2 * H * n_tokens_any + ((H + 4) * n_kept if fp8 else 2 * H * n_kept)
     return {
         "route_bytes": 2 * T * H + 2 * H * E + 8 * T * k,
         "route_flop": 2 * T * H * E,
-        "permute_bytes": 2 * H * (n_tokens_any + n_kept),
+        "permute_bytes": permute,
         "gemm1_flop": 2 * n_kept * H * h,
         "gemm2_flop": 2 * n_kept * h * H,
         "combine_bytes": 2 * H * (n_kept + T),
@@ -261,7 +264,7 @@ def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
 def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2):
     T, k = w.T, w.k
     pk = peaks()
-    work = algorithmic_work(w, n_kept, any_kept)
+    work = algorithmic_work(w, n_kept, any_kept, fp8=args.fp8)
     names = ["route", "scan", "permute", "gemm1", "gemm2", "combine"]
     stage = dict(zip(names, stage_ms))
     kern = {}
