@@ -10,10 +10,11 @@
 // expert with an odd m-tile count leaves the last pair's second half past
 // the segment end; its rows are computed and never stored.
 //
-// Roles per CTA (192 threads): warp 0 = TMA producer (both CTAs, own halves,
+// Roles per CTA (320 threads): warp 0 = TMA producer (both CTAs, own halves,
 // transaction bytes counted on the leader's barrier); warp 1 = UMMA issuer
-// (leader only) and TMEM allocation (both, collectively); warps 2-5 =
-// epilogue of the CTA's own 128 rows. Stage and accumulator barriers are
+// (leader only) and TMEM allocation (both, collectively); warps 2-9 =
+// epilogue of the CTA's own 128 rows, two warps per TMEM lane quadrant, each
+// taking half of the 256 columns. Stage and accumulator barriers are
 // released to both CTAs by multicast commits; the leader waits for both
 // epilogues before reusing an accumulator.
 #include "moe_internal.h"
@@ -26,7 +27,8 @@ namespace {
 constexpr int kBM = 128;           // rows per CTA; the pair computes 256
 constexpr int kBN = 256;           // columns per pair tile (128 held by each CTA)
 constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                             // 2 per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBlockK * 2;          // 16 KB
 constexpr uint32_t kBBytes = (kBN / 2) * kBlockK * 2;    // 16 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 32 KB
@@ -76,7 +78,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kKE = kFp8 ? 128 : kBlockK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // FP8 column scales of the current tile, 128 per epilogue warp
+  float* col_scale = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(col_scale + kEpiWarps * (kBN / 2));
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * 4 * 32);  // both CTAs' epilogue threads
+      mbar_init(&tempty[a], 2 * kEpiWarps * 32);  // both CTAs' epilogue threads
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -270,63 +274,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------ epilogue ----
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // warp w reads TMEM lane quadrant w % 4 (the only one it may access) and
+    // columns [128*half, 128*half + 128) of the accumulator
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    float* wscale = col_scale + (warp - 2) * (kBN / 2);
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                        mapa_shared(smem_u32(&tempty[1]), 0)};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = cluster; L < total; L += n_clusters) {
       const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
-      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
-      tc_fence_after();
       const int row = c.row0 + 32 * q + lane;
       const bool valid = row < c.row_end;
+      const int col0 = c.n0 + half * (kBN / 2);
+      // whole 32-column chunks: N is a multiple of 64
+      const int n_chunks = col0 >= p.N ? 0 : min(4, (p.N - col0) / 32);
+      float rs = 1.f;
+      if constexpr (kFp8) {
+        // scales are fetched before the accumulator wait, hiding their latency
+        __syncwarp();  // the previous tile's reads of wscale are done
+        const int col = col0 + 4 * lane;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < p.N)
+          v = *reinterpret_cast<const float4*>(p.b_scale + static_cast<size_t>(c.e) * p.N + col);
+        reinterpret_cast<float4*>(wscale)[lane] = v;
+        if (valid) rs = p.a_scale[row];
+        __syncwarp();
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      tc_fence_after();
       uint16_t* drow = p.D + static_cast<size_t>(valid ? row : 0) * p.N;
-      float row_max = 0.f;  // FP8 mode: max |output| of this row in this tile
-      const uint32_t t_base =
-          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * kBN);
-#pragma unroll 1
-      for (int cc = 0; cc < kBN / 32; ++cc) {
-        const int col = c.n0 + 32 * cc;
-        if (col >= p.N) break;  // N is a multiple of 64: whole chunks
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_base + 32u * cc, r);
+      float row_max = 0.f;  // FP8 mode: max |output| of this row in these columns
+      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                              static_cast<uint32_t>(acc * kBN + half * (kBN / 2));
+      // two register sets: the next chunk's TMEM load overlaps this chunk's math
+      uint32_t ra[32], rb[32];
+      if (n_chunks > 0) {
+        tmem_ld_32x32b_x32(t_base, ra);
         tmem_ld_wait();
-        if (valid) {
-          uint32_t packed[16];
-          float rs = 1.f;
-          const float* cs = nullptr;
-          if constexpr (kFp8) {
-            rs = p.a_scale[row];
-            cs = p.b_scale + static_cast<size_t>(c.e) * p.N + col;
-          }
+      }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = __uint_as_float(r[2 * i]);
-            float v1 = __uint_as_float(r[2 * i + 1]);
-            if constexpr (kFp8) {
-              v0 = v0 * rs * cs[2 * i];
-              v1 = v1 * rs * cs[2 * i + 1];
-            }
-            if (p.gelu) {
-              v0 = gelu_tanh_f(v0);
-              v1 = gelu_tanh_f(v1);
-            }
-            if constexpr (kFp8) row_max = fmaxf(row_max, fmaxf(fabsf(v0), fabsf(v1)));
-            packed[i] = pack_bf16x2(v0, v1);
-          }
-          // outputs are read once, by the next kernel: stream them past L2
-          uint4* dst = reinterpret_cast<uint4*>(drow + col);
+      for (int cc = 0; cc < 4; ++cc) {
+        if (cc < n_chunks) {
+          uint32_t(&r)[32] = (cc & 1) ? rb : ra;
+          uint32_t(&nx)[32] = (cc & 1) ? ra : rb;
+          if (cc + 1 < n_chunks) tmem_ld_32x32b_x32(t_base + 32u * (cc + 1), nx);
+          if (valid) {
+            uint32_t packed[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                                packed[4 * i + 3]));
+            for (int i = 0; i < 16; ++i) {
+              float v0 = __uint_as_float(r[2 * i]);
+              float v1 = __uint_as_float(r[2 * i + 1]);
+              if constexpr (kFp8) {
+                v0 = v0 * rs * wscale[32 * cc + 2 * i];
+                v1 = v1 * rs * wscale[32 * cc + 2 * i + 1];
+              }
+              if (p.gelu) {
+                v0 = gelu_tanh_f(v0);
+                v1 = gelu_tanh_f(v1);
+              }
+              if constexpr (kFp8) row_max = fmaxf(row_max, fmaxf(fabsf(v0), fabsf(v1)));
+              packed[i] = pack_bf16x2(v0, v1);
+            }
+            // outputs are read once, by the next kernel: stream them past L2
+            uint4* dst = reinterpret_cast<uint4*>(drow + col0 + 32 * cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1],
+                                                  packed[4 * i + 2], packed[4 * i + 3]));
+          }
+          if (cc + 1 < n_chunks) tmem_ld_wait();
         }
       }
       if constexpr (kFp8) {
         // bf16 rounding is monotonic, so the rounded maximum is the maximum
         // of the rounded (stored) values
-        if (p.row_amax != nullptr && valid && c.n0 < p.N)
+        if (p.row_amax != nullptr && valid && n_chunks > 0)
           atomicMax(p.row_amax + row, __float_as_uint(bf16_lo(pack_bf16x2(row_max, 0.f))));
       }
       tc_fence_before();
@@ -349,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t gemm_pair_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 8 * (2 * kStages + 5) + 16 +
-         8 * static_cast<size_t>(E + 1);
+  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiWarps * (kBN / 2) +
+         8 * (2 * kStages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
 template <bool kFp8>
