@@ -256,8 +256,12 @@ __device__ __forceinline__ void cluster_sync() {
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly in
 // the peer CTA).
+// Relaxed: the arrive orders nothing in generic memory. Used where the waiter
+// only needs the arriving thread's tcgen05 reads to be complete (wait::ld
+// plus tcgen05.fence::before_thread_sync on this side), so the arrive does
+// not wait for the thread's earlier global stores to become visible.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 
