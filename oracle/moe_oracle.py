@@ -45,6 +45,9 @@ R11 Training router (Gumbel): z = (logits + g)/tau with g from caller-drawn
     uniforms; top-k on z, weights and balance statistics from softmax(z).
 R12 FP8 path: e4m3 with per-token-row scales for activations and
     per-output-column scales for weights, formed in fp32 (see the FP8 section).
+    The expert outputs on their way to the combine are e4m3 with one scale
+    per 128-column block of each row (the last block of a row may be
+    narrower), formed from the bf16-rounded outputs.
 
 Parity pins for every function here live in tests/test_oracle_pins.py.
 """
@@ -393,10 +396,37 @@ def expert_mlp_fp8(xq: np.ndarray, xs: np.ndarray, w1q, w1s, w2q, w2s) -> np.nda
     return bf16_round(y)
 
 
-def token_outputs_fp8(x_rows, idx_rows, w_rows, kept_rows, Q1, Q2) -> np.ndarray:
+FP8_BLOCK = 128
+
+
+def quantize_blocks_fp8(a: np.ndarray, block: int = FP8_BLOCK):
+    """Per-(row, column block) e4m3 quantisation: each run of `block`
+    columns of a row (the last one may be narrower) is quantised as
+    quantize_rows_fp8 quantises a row. Returns (q as float64 [n, m], scales
+    as float64 [n, ceil(m / block)])."""
+    a = np.asarray(a)
+    n, m = a.shape
+    nb = -(-m // block)
+    q = np.zeros((n, m), np.float64)
+    s = np.zeros((n, nb), np.float64)
+    for b in range(nb):
+        q[:, b * block:(b + 1) * block], s[:, b] = quantize_rows_fp8(a[:, b * block:(b + 1) * block])
+    return q, s
+
+
+def dequantize_blocks_fp8(q: np.ndarray, s: np.ndarray, block: int = FP8_BLOCK) -> np.ndarray:
+    """q * scale of its block, as float64."""
+    cols = np.arange(q.shape[1]) // block
+    return np.asarray(q, np.float64) * np.asarray(s, np.float64)[:, cols]
+
+
+def token_outputs_fp8(x_rows, idx_rows, w_rows, kept_rows, Q1, Q2,
+                      fp8_combine: bool = False) -> np.ndarray:
     """y for a subset of tokens through the FP8 FFN: each token row is
     quantised once (the dispatch), then every kept expert runs
-    expert_mlp_fp8; Q1[e] = (w1q, w1s), Q2[e] = (w2q, w2s)."""
+    expert_mlp_fp8; Q1[e] = (w1q, w1s), Q2[e] = (w2q, w2s). With
+    fp8_combine the expert outputs reach the combine as 128-column block
+    quantised e4m3 (quantize_blocks_fp8) and are dequantised there."""
     x_rows = np.asarray(x_rows, np.float64)
     n, H = x_rows.shape
     xq, xs = quantize_rows_fp8(x_rows)
@@ -409,6 +439,8 @@ def token_outputs_fp8(x_rows, idx_rows, w_rows, kept_rows, Q1, Q2) -> np.ndarray
                 w1q, w1s = Q1[int(e)]
                 w2q, w2s = Q2[int(e)]
                 ye = expert_mlp_fp8(xq[sel], xs[sel], w1q, w1s, w2q, w2s)
+                if fp8_combine:
+                    ye = dequantize_blocks_fp8(*quantize_blocks_fp8(ye))
                 acc[sel] += np.asarray(w_rows)[sel, j][:, None] * ye
     return bf16_round(acc)
 

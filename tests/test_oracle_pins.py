@@ -515,3 +515,68 @@ def test_fp8_ffn_close_to_bf16_ffn():
     # e4m3 keeps 4 significant bits: a few percent, well away from bf16 error
     rel = np.abs(y8 - y16).sum() / np.abs(y16).sum()
     assert 0.005 < rel < 0.08
+
+
+def test_block_quantisation_scales_each_block_alone():
+    # blocks of 128 columns, the last one 64 wide; magnitudes differ by 1e6
+    # between blocks, so one scale per row would crush the small blocks
+    a = rng.standard_normal((6, 320)).astype(np.float32)
+    a[:, :128] *= 1e-3
+    a[:, 128:256] *= 1e3
+    a[4, 256:] = 0.0
+    q, s = O.quantize_blocks_fp8(a)
+    assert q.shape == (6, 320) and s.shape == (6, 3)
+    for b, (lo, hi) in enumerate([(0, 128), (128, 256), (256, 320)]):
+        blk = a[:, lo:hi]
+        amax = np.abs(blk).max(axis=1).astype(np.float32)
+        nz = amax > 0
+        assert np.array_equal(s[nz, b], (amax[nz] / np.float32(448)).astype(np.float64))
+        inv = (np.float32(448) / amax[nz]).astype(np.float32)
+        ref = torch.from_numpy((blk[nz] * inv[:, None]).astype(np.float32)).to(
+            torch.float8_e4m3fn).to(torch.float64).numpy()
+        assert np.array_equal(q[nz, lo:hi], ref)
+        assert np.allclose(np.abs(q[nz, lo:hi]).max(axis=1), 448.0)
+    assert s[4, 2] == 0 and (q[4, 256:] == 0).all()
+    deq = O.dequantize_blocks_fp8(q, s)
+    rel = np.abs(deq - a) / np.maximum(np.abs(a), 1e-30)
+    # normal-range values of every block keep 4 significant bits
+    tiny = np.zeros_like(a, bool)
+    for lo, hi in [(0, 128), (128, 256), (256, 320)]:
+        m = np.abs(a[:, lo:hi]).max(axis=1, keepdims=True)
+        tiny[:, lo:hi] = np.abs(a[:, lo:hi]) * 448.0 / np.maximum(m, 1e-30) < 2 ** -6
+    assert (rel[~tiny & (a != 0)] <= 2.0 ** -4 * 1.0001).all()
+
+
+def test_block_quantisation_of_a_narrow_row_is_row_quantisation():
+    a = rng.standard_normal((5, 96))
+    q1, s1 = O.quantize_blocks_fp8(a)
+    q2, s2 = O.quantize_rows_fp8(a)
+    assert np.array_equal(q1, q2) and np.array_equal(s1[:, 0], s2)
+
+
+def test_fp8_combine_changes_outputs_by_at_most_an_e4m3_step():
+    H, h, E, k, n = 256, 128, 4, 2, 40
+    x = O.bf16_round(rng.standard_normal((n, H)))
+    W1 = [O.bf16_round(rng.standard_normal((H, h)) / 16) for _ in range(E)]
+    W2 = [O.bf16_round(rng.standard_normal((h, H)) / 11) for _ in range(E)]
+    Q1 = [O.quantize_weights_fp8(w) for w in W1]
+    Q2 = [O.quantize_weights_fp8(w) for w in W2]
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(n)])
+    w = rng.uniform(0.1, 1.0, (n, k))
+    kept = np.ones((n, k), bool)
+    kept[3, 1] = False
+    y = O.token_outputs_fp8(x, idx, w, kept, Q1, Q2)
+    y8 = O.token_outputs_fp8(x, idx, w, kept, Q1, Q2, fp8_combine=True)
+    assert not np.array_equal(y, y8)
+    # bound: half an e4m3 step (2^-4 relative) of each summed term, plus the
+    # final bf16 rounding of both results
+    xq, xs = O.quantize_rows_fp8(x)
+    bound = np.zeros((n, H))
+    for t in range(n):
+        for j in range(k):
+            if kept[t, j]:
+                e = idx[t, j]
+                ye = O.expert_mlp_fp8(xq[t:t + 1], xs[t:t + 1], *Q1[e], *Q2[e])[0]
+                bound[t] += w[t, j] * np.abs(ye)
+    bound = 2.0 ** -4 * bound + 2.0 ** -7 * (np.abs(y) + np.abs(y8))
+    assert (np.abs(y8 - y) <= bound + 1e-30).all()

@@ -2,7 +2,7 @@
 // product as grouped_gemm_kernel (D[r,:] = A[r,:] . B[e(r)], optional GELU)
 // with a 2-CTA UMMA (cta_group::2, M=256, N=256). Each CTA of a cluster pair
 // holds its own 128 rows of A and its own 128 columns of B per stage, so a
-// stage is 32 KB instead of 48 KB: six stages fit, and shared memory moves
+// stage is 32 KB instead of 48 KB: six or seven stages fit, and shared memory moves
 // a third less data per FLOP than the single-CTA kernel.
 //
 // A pair tile is (expert e, pair index pm, n-tile): CTA rank r computes the
@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kBM = 128;           // rows per CTA; the pair computes 256
 constexpr int kBN = 256;           // columns per pair tile (128 held by each CTA)
-constexpr int kStages = 6;
+constexpr int kMaxStages = 7;  // bf16 with E <= 234; FP8 (scale area) and larger E: 6
 constexpr int kEpiWarps = 8;                             // 2 per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBlockK * 2;          // 16 KB
@@ -78,11 +78,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kKE = kFp8 ? 128 : kBlockK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
+  const int nst = p.stages;  // pipeline depth, chosen by the launcher to fit shared memory
   // FP8 column scales of the current tile, 128 per epilogue warp
-  float* col_scale = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(col_scale + kEpiWarps * (kBN / 2));
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  float* col_scale = reinterpret_cast<float*>(smem + nst * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(col_scale + (kFp8 ? kEpiWarps * (kBN / 2) : 0));
+  uint64_t* empty = full + nst;
+  uint64_t* tfull = empty + nst;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish_pair();
   }
   if (warp == 2 && lane == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                b_row + kb * kBlockK);
           }
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -200,9 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // barriers count both CTAs' bytes)
           int s = stage;
           uint32_t ph = phase;
-          for (int d = 0; d < kStages && d < issued; ++d) {
+          for (int d = 0; d < nst && d < issued; ++d) {
             if (--s < 0) {
-              s = kStages - 1;
+              s = nst - 1;
               ph ^= 1u;
             }
             mbar_wait_drain(&full[s], ph, kDrainLimitNs);
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           umma_commit_pair_multicast(&empty[stage], 0x3);
-          if (++stage == kStages) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -372,16 +373,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t gemm_pair_smem_bytes(int E) {
-  return 1024 + static_cast<size_t>(kStages) * kStageBytes + 4 * kEpiWarps * (kBN / 2) +
-         8 * (2 * kStages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
+size_t gemm_pair_smem_bytes(int E, int stages, bool fp8) {
+  return 1024 + static_cast<size_t>(stages) * kStageBytes + (fp8 ? 4 * kEpiWarps * (kBN / 2) : 0) +
+         8 * (2 * stages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
 template <bool kFp8>
 cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
                         int num_sms, cudaStream_t st) {
-  const size_t smem = gemm_pair_smem_bytes(a.E);
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8>,
+  // the deepest ring that fits: every stage in flight hides TMA latency
+  int dev = 0, optin = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  GemmArgs args = a;
+  args.stages = kMaxStages;
+  while (args.stages > 2 && gemm_pair_smem_bytes(a.E, args.stages, kFp8) > static_cast<size_t>(optin))
+    --args.stages;
+  const size_t smem = gemm_pair_smem_bytes(a.E, args.stages, kFp8);
+  err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -397,7 +408,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8>, tm_a, tm_b, a);
+  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8>, tm_a, tm_b, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

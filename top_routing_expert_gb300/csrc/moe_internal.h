@@ -98,6 +98,7 @@ struct GemmArgs {
   const float* b_scale;    // FP8 mode: per-column scales of B [E, N]
   uint32_t* row_amax;      // FP8 mode, optional: max |bf16 output| per row, fp32 bits,
                            // combined with atomicMax (zeroed by the caller)
+  int stages;              // CTA-pair kernel: pipeline depth (set by its launcher)
   uint32_t* dev_status;
   uint64_t timeout_ns;
 };
@@ -120,7 +121,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b
                                 const GemmArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st);
-size_t gemm_pair_smem_bytes(int E);
+size_t gemm_pair_smem_bytes(int E, int stages, bool fp8);
 cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                          const GemmArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, int E, int K,
