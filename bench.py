@@ -62,16 +62,18 @@ def algorithmic_work(w: W.Workload, n_kept: int, n_tokens_any: int, fp8: bool = 
     removed); GEMM1/GEMM2 are 2*N*H*h FLOP each (4*H*h per token-expert,
     section 2.2); combine reads each kept row and writes each token row.
     With FP8 the permute writes e4m3 rows (1 byte per value) and a 4-byte
-    scale per kept row."""
+    scale per kept row, and the combine reads e4m3 rows with a 4-byte scale
+    per 128-column block."""
     T, H, E, k, h = w.T, w.H, w.E, w.k, w.h
     permute = 2 * H * n_tokens_any + ((H + 4) * n_kept if fp8 else 2 * H * n_kept)
+    combine_in = (H + 4 * -(-H // 128)) * n_kept if fp8 else 2 * H * n_kept
     return {
         "route_bytes": 2 * T * H + 2 * H * E + 8 * T * k,
         "route_flop": 2 * T * H * E,
         "permute_bytes": permute,
         "gemm1_flop": 2 * n_kept * H * h,
         "gemm2_flop": 2 * n_kept * h * H,
-        "combine_bytes": 2 * H * (n_kept + T),
+        "combine_bytes": combine_in + 2 * H * T,
     }
 
 
@@ -311,7 +313,8 @@ def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2
         "config": {**w.describe(), "parallelism": f"replicas x{world} (no exchange)",
                    "router": "inference (top-k of logits)" if args.gumbel is None
                    else f"training (Gumbel noise, temperature {args.gumbel})",
-                   "expert_ffn": "FP8 e4m3 dispatch + FFN, per-row/per-column fp32 scales"
+                   "expert_ffn": "FP8 e4m3 dispatch + FFN + combine, per-row/per-column/"
+                                 "128-column-block fp32 scales"
                    if args.fp8 else "bf16",
                    "l2": l2},
         "clocks": clk,

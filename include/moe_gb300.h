@@ -275,19 +275,35 @@ MOE_API moe_status moe_permute_fp8(const moe_shape* s, const moe_bf16* x, const 
 
 /* moe_expert_ffn on e4m3 rows: u = x_scale[r] * w1_scale[e,:] * (x_q[r] .
  * W1q[e]^T) in fp32; act [T*k,h] bf16 = bf16(gelu_tanh(u)); act is
- * quantised per row (scale from the largest |act| of the row) and
- * y_perm [T*k,H] bf16 = bf16(act_scale[r] * w2_scale[e,:] * (act_q[r] .
- * W2q[e]^T)). ws must hold moe_workspace_size_fp8 bytes. */
+ * quantised per row (scale from the largest |act| of the row) and the
+ * expert outputs are v = bf16(act_scale[r] * w2_scale[e,:] * (act_q[r] .
+ * W2q[e]^T)), written either
+ *   - as y_perm [T*k,H] bf16 (y_q, y_scale NULL), or
+ *   - as y_q [T*k,H] e4m3 with y_scale [T*k, ceil(H/128)] fp32, one scale per
+ *     128-column block of a row formed from the bf16 values v like a row
+ *     scale (y_perm NULL): the FP8 payload of the combine.
+ * Both y_perm and y_q given returns MOE_ERR_UNSUPPORTED. ws must hold
+ * moe_workspace_size_fp8 bytes. */
 MOE_API moe_status moe_expert_ffn_fp8(const moe_shape* s, const uint8_t* x_q, const float* x_scale,
                               const int32_t* offsets, const uint8_t* W1q, const float* w1_scale,
                               const uint8_t* W2q, const float* w2_scale, moe_bf16* act,
-                              moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
-                              void* stream);
+                              moe_bf16* y_perm, uint8_t* y_q, float* y_scale,
+                              uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 
-/* moe_layer_fwd with the FP8 dispatch and FP8 expert FFN (weights from
- * moe_quantize_weights_fp8); the router and the combine are those of
- * moe_layer_fwd. ws must hold moe_workspace_size_fp8 bytes. events as in
- * moe_layer_fwd, events[4] recorded after GEMM1 and the act quantisation. */
+/* moe_combine on the e4m3 expert outputs of moe_expert_ffn_fp8:
+ * y[t] = bf16(sum over kept slots j, ascending, of topk_w[t,j] *
+ * y_q[r,c] * y_scale[r, c/128]), r = dest_row[t,j], fp32 accumulation. The
+ * combine's FP8 half of the comm bottleneck page, section 5.3. Needs no
+ * workspace. */
+MOE_API moe_status moe_combine_fp8(const moe_shape* s, const uint8_t* y_q, const float* y_scale,
+                           const int32_t* dest_row, const float* topk_w, moe_bf16* y,
+                           void* stream);
+
+/* moe_layer_fwd with the FP8 dispatch, the FP8 expert FFN (weights from
+ * moe_quantize_weights_fp8) and the FP8 combine (expert outputs as e4m3
+ * with 128-column block scales); the router is that of moe_layer_fwd. ws
+ * must hold moe_workspace_size_fp8 bytes. events as in moe_layer_fwd,
+ * events[4] recorded after GEMM1 and the act quantisation. */
 MOE_API moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,
                              const float* gate_bias, const uint8_t* W1q, const float* w1_scale,
                              const uint8_t* W2q, const float* w2_scale, moe_bf16* y, float* aux,

@@ -200,7 +200,16 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
                                  f, n, None, None) == 4
     assert lib.moe_layer_fwd_fp8(ctypes.byref(s), f, f, None, f, None, f, f, f, *[None] * 9,
                                  f, n8.value, None, None) == 1
-    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, None, f, f, f, f, f, f, f, None, f,
-                                  n8.value, None) == 1
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, None, f, f, f, f, f, f, f, None, None,
+                                  None, f, n8.value, None) == 1
+    # outputs: bf16 y_perm, or e4m3 y_q with y_scale - not both, not neither
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, f, f, f, f, f, f, f, f, f, f,
+                                  None, f, n8.value, None) == 3
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, f, f, f, f, f, f, f, None, f, None,
+                                  None, f, n8.value, None) == 1
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(s), f, f, f, f, f, f, f, f, None, None, None,
+                                  None, f, n8.value, None) == 1
+    assert lib.moe_combine_fp8(ctypes.byref(s), f, None, f, f, f, None) == 1
+    assert lib.moe_combine_fp8(ctypes.byref(s), f, P(FAKE + 4), f, f, f, None) == 5
     assert lib.moe_permute_fp8(ctypes.byref(s), f, f, None, f, f, None, f, None, None, f, n,
                                None) == 1

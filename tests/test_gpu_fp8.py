@@ -12,7 +12,8 @@ import torch
 import top_routing_expert_gb300 as moe
 import workloads as W
 from oracle import moe_oracle as O
-from tests._helpers import NEAR_TIE, assert_ffn_close, fill_nan_bf16, np64, oracle_logits_chunked, topk_margins
+from tests._helpers import (NEAR_TIE, assert_ffn_close, assert_fp8_out_close, fill_nan_bf16, np64,
+                            oracle_logits_chunked, topk_margins)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -174,10 +175,29 @@ def test_expert_ffn_fp8_against_oracle(E, H, h, counts):
     act = _zeros((A, h), torch.bfloat16)
     yp = _zeros((A, H), torch.bfloat16)
     st = _status()
-    moe.moe_expert_ffn_fp8(s, xq.to(DEV), xs.to(DEV), torch.from_numpy(off).to(DEV), Q, act, yp,
-                           st, ws)
+    moe.moe_expert_ffn_fp8(s, xq.to(DEV), xs.to(DEV), torch.from_numpy(off).to(DEV), Q, act,
+                           y_perm=yp, dev_status=st, ws=ws)
+    # the same FFN with e4m3 outputs and 128-column block scales
+    yq = torch.full((A, H), 0x7F, dtype=torch.uint8, device=DEV)
+    ysc = torch.full((A, (H + 127) // 128), -1.0, device=DEV)
+    act2 = _zeros((A, h), torch.bfloat16)
+    moe.moe_expert_ffn_fp8(s, xq.to(DEV), xs.to(DEV), torch.from_numpy(off).to(DEV), Q, act2,
+                           y_q=yq, y_scale=ysc, dev_status=st, ws=ws)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+    assert torch.equal(act2[:N].cpu(), act[:N].cpu())
+    # property: the block quantisation of this run's own bf16 outputs (the
+    # definition: amax of the block, 448/amax in fp32, e4m3 round to even)
+    yb = yp[:N].float().cpu()
+    nb = (H + 127) // 128
+    amax = torch.stack([yb[:, 128 * b:128 * (b + 1)].abs().amax(dim=1) for b in range(nb)], dim=1)
+    assert torch.equal(ysc[:N].cpu(), amax / 448.0)
+    # a true fp32 division (torch evaluates `scalar / tensor` as a reciprocal
+    # times the scalar, which is not the correctly rounded quotient)
+    inv = torch.where(amax > 0, torch.full_like(amax, 448.0) / amax, torch.zeros_like(amax))
+    cols = torch.arange(H) // 128
+    want = (yb * inv[:, cols]).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(yq[:N].cpu(), want)
     ref_act = np.zeros((N, h))
     ref_y = np.zeros((N, H))
     for e in range(E):
@@ -188,6 +208,9 @@ def test_expert_ffn_fp8_against_oracle(E, H, h, counts):
             ref_y[a:b] = O.expert_mlp_fp8(xq64[a:b], xs64[a:b], *Q1[e], *Q2[e])
     assert_ffn_close(np64(act[:N]), ref_act, "act")
     assert_ffn_close(np64(yp[:N]), ref_y, "y_perm")
+    deq = O.dequantize_blocks_fp8(e4m3_values(yq[:N]), ysc[:N].cpu().numpy().astype(np.float64))
+    assert_fp8_out_close(deq, O.dequantize_blocks_fp8(*O.quantize_blocks_fp8(ref_y)),
+                         "y_q (dequantised)")
 
 
 # ========================================================= layer ====
@@ -248,8 +271,8 @@ def _check_layer_fp8(w, inp, g, Q, sample=None, check_experts=None):
     rows = rows[same]
     kept = d.dest_row[rows] >= 0
     ref = O.token_outputs_fp8(np64(inp["x"][torch.from_numpy(rows)]), r.idx[rows], r.w[rows], kept,
-                              _LazyQ(inp["W1"]), _LazyQ(inp["W2"]))
-    assert_ffn_close(np64(g["y"][torch.from_numpy(rows)]), ref, f"{w.name} fp8 y")
+                              _LazyQ(inp["W1"]), _LazyQ(inp["W2"]), fp8_combine=True)
+    assert_fp8_out_close(np64(g["y"][torch.from_numpy(rows)]), ref, f"{w.name} fp8 y")
 
 
 @pytest.mark.parametrize("name", ["tiny", "imbalanced"])
@@ -275,7 +298,8 @@ def test_layer_fp8_edge_shapes(T, H, E, k, h, cf, bias):
 
 def test_layer_fp8_deterministic_and_chain():
     """Two layer calls give the same bits, and permute_fp8 -> expert_ffn_fp8
-    -> combine through the separate entry points gives them too."""
+    (e4m3 outputs) -> combine_fp8 through the separate entry points gives
+    them too."""
     w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="fp8chain")
     inp = W.make_inputs(w, seed=5)
     g1, Q = _layer_fp8_gpu(w, inp)
@@ -295,10 +319,11 @@ def test_layer_fp8_deterministic_and_chain():
     xs = _zeros(A, torch.float32)
     moe.moe_permute_fp8(s, dv["x"], idx, None, off, dest, None, xq, xs, ws=ws)
     act = _zeros((A, w.h), torch.bfloat16)
-    yp = _zeros((A, w.H), torch.bfloat16)
-    moe.moe_expert_ffn_fp8(s, xq, xs, off, Q, act, yp, ws=ws)
+    yq = _zeros((A, w.H), torch.uint8)
+    ysc = _zeros((A, (w.H + 127) // 128), torch.float32)
+    moe.moe_expert_ffn_fp8(s, xq, xs, off, Q, act, y_q=yq, y_scale=ysc, ws=ws)
     y = _zeros((T, w.H), torch.bfloat16)
-    moe.moe_combine(s, yp, dest, wt, y)
+    moe.moe_combine_fp8(s, yq, ysc, dest, wt, y)
     torch.cuda.synchronize()
     assert torch.equal(dest.cpu(), g1["dest_row"])
     assert torch.equal(y.cpu(), g1["y"])
@@ -338,7 +363,38 @@ def test_fp8_nan_rows_past_the_kept_rows_do_not_leak():
     fill_nan_bf16(act)
     yp = _zeros((T * k, H), torch.bfloat16)
     off = torch.tensor([0, 130, 135], dtype=torch.int32)
-    moe.moe_expert_ffn_fp8(s, xq.to(DEV), xs.to(DEV), off.to(DEV), Q, act, yp, ws=ws)
+    moe.moe_expert_ffn_fp8(s, xq.to(DEV), xs.to(DEV), off.to(DEV), Q, act, y_perm=yp, ws=ws)
     torch.cuda.synchronize()
     assert torch.isfinite(yp[:N].float()).all()
     assert torch.isfinite(act[:N].float()).all()
+
+
+# ======================================================= combine ====
+
+@pytest.mark.parametrize("T,H,k,drop", [(512, 256, 2, 0.0), (1000, 320, 3, 0.3), (77, 64, 8, 0.5),
+                                        (4096, 4096, 2, 0.01), (300, 2048, 6, 0.1)])
+def test_combine_fp8_against_oracle(T, H, k, drop):
+    gen = torch.Generator().manual_seed(T + k + 1)
+    N = T * k
+    perm = torch.randperm(N, generator=gen).reshape(T, k).to(torch.int32)
+    dropm = torch.rand((T, k), generator=gen) < drop
+    dest = torch.where(dropm, torch.full_like(perm, -1), perm)
+    w = W.make_weights(T, k, seed=T)
+    yb = torch.randn((N, H), generator=gen).to(torch.bfloat16)
+    yb[:, :64] *= 1e-3                                  # a small block beside large ones
+    q, sc = O.quantize_blocks_fp8(np64(yb))
+    y = _zeros((T, H), torch.bfloat16)
+    fill_nan_bf16(y)
+    moe.moe_combine_fp8(moe.MoeShape.make(T, H, max(k, 1), k, 64, 1.0), e4m3_bytes(q).to(DEV),
+                        torch.from_numpy(sc.astype(np.float32)).to(DEV), dest.to(DEV), w.to(DEV), y)
+    torch.cuda.synchronize()
+    d = O.Dispatch(C=0, pos=None, kept_counts=None, offsets=None, dest_row=dest.numpy(),
+                   src_token=None, N=N)
+    w64 = w.numpy().astype(np.float64)
+    deq = O.dequantize_blocks_fp8(q, sc)
+    ref = O.combine(deq, d, w64, H)
+    got = np64(y.cpu())
+    mag = O.combine(np.abs(deq), d, np.abs(w64), H)
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + mag * 2.0 ** -20).all()
+    assert np.mean(got == ref) > 0.98
+    assert (got[(dest.numpy() < 0).all(axis=1)] == 0).all()

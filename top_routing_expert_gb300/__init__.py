@@ -23,7 +23,7 @@ __all__ = [
     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
     "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
     "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
-    "moe_layer_fwd_fp8", "Fp8Weights",
+    "moe_layer_fwd_fp8", "moe_combine_fp8", "Fp8Weights",
     "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
@@ -35,7 +35,8 @@ EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "mo
                     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc",
                     "moe_host_workspace_size", "moe_layer_fwd_host", "moe_route_gumbel",
                     "moe_layer_fwd_gumbel", "moe_workspace_size_fp8", "moe_quantize_weights_fp8",
-                    "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8"]
+                    "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8",
+                    "moe_combine_fp8"]
 
 
 class MoeError(RuntimeError):
@@ -104,7 +105,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_permute_fp8.restype = ctypes.c_int
     lib.moe_permute_fp8.argtypes = [S] + [_P] * 10 + [ctypes.c_size_t, _P]
     lib.moe_expert_ffn_fp8.restype = ctypes.c_int
-    lib.moe_expert_ffn_fp8.argtypes = [S] + [_P] * 11 + [ctypes.c_size_t, _P]
+    lib.moe_expert_ffn_fp8.argtypes = [S] + [_P] * 13 + [ctypes.c_size_t, _P]
+    lib.moe_combine_fp8.restype = ctypes.c_int
+    lib.moe_combine_fp8.argtypes = [S] + [_P] * 6
     lib.moe_layer_fwd_fp8.restype = ctypes.c_int
     lib.moe_layer_fwd_fp8.argtypes = [S] + [_P] * 18 + [ctypes.c_size_t, _P, _P]
     _lib = lib
@@ -428,9 +431,12 @@ def moe_permute_fp8(shape, x, topk_idx, kept_counts, offsets, dest_row, src_toke
         _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
 
 
-def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm,
-                       dev_status=None, ws: Workspace | None = None, stream=None):
-    """Expert FFN on e4m3 rows; ws must be an fp8=True workspace."""
+def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm=None,
+                       y_q=None, y_scale=None, dev_status=None, ws: Workspace | None = None,
+                       stream=None):
+    """Expert FFN on e4m3 rows; outputs bf16 y_perm, or e4m3 y_q [T*k,H]
+    (uint8) with y_scale [T*k, ceil(H/128)] block scales. ws must be an
+    fp8=True workspace."""
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn_fp8", load_library().moe_expert_ffn_fp8(
@@ -438,8 +444,18 @@ def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm,
         _ptr(offsets, torch.int32, "offsets"), _ptr(q.W1q, torch.uint8, "W1q"),
         _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
         _ptr(q.w2_scale, torch.float32, "w2_scale"), _ptr(act, torch.bfloat16, "act"),
-        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(y_q, torch.uint8, "y_q"),
+        _ptr(y_scale, torch.float32, "y_scale"), _ptr(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
+
+
+def moe_combine_fp8(shape, y_q, y_scale, dest_row, topk_w, y, stream=None):
+    """Combine of e4m3 expert outputs with 128-column block scales."""
+    s = _shape(shape)
+    _check("moe_combine_fp8", load_library().moe_combine_fp8(
+        ctypes.byref(s), _ptr(y_q, torch.uint8, "y_q"), _ptr(y_scale, torch.float32, "y_scale"),
+        _ptr(dest_row, torch.int32, "dest_row"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(y, torch.bfloat16, "y"), _stream(stream)))
 
 
 def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, topk_idx=None,

@@ -81,6 +81,7 @@ struct Ws {
   uint8_t* act_q;
   float* act_scale;
   uint32_t* act_amax;
+  float* y_scale;  // block scales of the e4m3 expert outputs (which live in the y_perm bytes)
 };
 
 struct Dims {
@@ -137,11 +138,13 @@ size_t layout(const Dims& d, uint8_t* base, Ws* w, bool fp8 = false) {
   v.act_q = nullptr;
   v.act_scale = nullptr;
   v.act_amax = nullptr;
+  v.y_scale = nullptr;
   if (fp8) {
     v.x_scale = static_cast<float*>(take(A * 4));
     v.act_q = static_cast<uint8_t*>(take(A * d.h));
     v.act_scale = static_cast<float*>(take(A * 4));
     v.act_amax = static_cast<uint32_t*>(take(A * 4));
+    v.y_scale = static_cast<float*>(take(A * static_cast<size_t>((d.H + 127) / 128) * 4));
   }
   if (w) *w = v;
   return off;
@@ -384,6 +387,8 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.a_scale = nullptr;
   g.b_scale = nullptr;
   g.row_amax = nullptr;
+  g.Dq = nullptr;
+  g.d_scale = nullptr;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   if (d.A >= kPairGemmMinRows)
@@ -399,7 +404,7 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
 moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
                         const uint8_t* Wq, const float* w_scale, const int32_t* offsets, int K,
                         int N, moe_bf16* D, int gelu, uint32_t* row_amax, uint32_t* status,
-                        cudaStream_t st) {
+                        cudaStream_t st, uint8_t* Dq = nullptr, float* d_scale = nullptr) {
   if (d.A == 0) return MOE_OK;
   CUtensorMap tm_a, tm_b;
   if (!tmap_u8_2d(&tm_a, Aq, K, d.A)) return MOE_ERR_CUDA;
@@ -415,6 +420,8 @@ moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
   g.a_scale = a_scale;
   g.b_scale = w_scale;
   g.row_amax = row_amax;
+  g.Dq = Dq;
+  g.d_scale = d_scale;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   MOE_CUDA(launch_grouped_gemm_pair_fp8(tm_a, tm_b, g, num_sms(), st));
@@ -422,11 +429,13 @@ moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
 }
 
 // FP8 expert FFN on dispatched e4m3 rows: GEMM1 (+GELU, row maxima of act),
-// act quantised per row, GEMM2.
+// act quantised per row, GEMM2 into bf16 y_perm or, with y_q, into e4m3
+// with 128-column block scales.
 moe_status run_ffn_fp8(const Dims& d, const uint8_t* xq, const float* xs, const int32_t* offsets,
                        const uint8_t* W1q, const float* w1s, const uint8_t* W2q,
                        const float* w2s, moe_bf16* act, moe_bf16* y_perm, uint32_t* status,
-                       const Ws& w, cudaStream_t st, void* const* events) {
+                       const Ws& w, cudaStream_t st, void* const* events,
+                       uint8_t* y_q = nullptr, float* y_scale = nullptr) {
   if (d.A == 0) return MOE_OK;
   MOE_CUDA(cudaMemsetAsync(w.act_amax, 0, sizeof(uint32_t) * static_cast<size_t>(d.A), st));
   MOE_TRY(run_gemm_fp8(d, xq, xs, W1q, w1s, offsets, d.H, d.h, act, 1, w.act_amax, status, st));
@@ -435,7 +444,22 @@ moe_status run_ffn_fp8(const Dims& d, const uint8_t* xq, const float* xs, const 
   if (events && cudaEventRecord(static_cast<cudaEvent_t>(events[0]), st) != cudaSuccess)
     return MOE_ERR_CUDA;
   MOE_TRY(run_gemm_fp8(d, w.act_q, w.act_scale, W2q, w2s, offsets, d.h, d.H, y_perm, 0, nullptr,
-                       status, st));
+                       status, st, y_q, y_scale));
+  return MOE_OK;
+}
+
+moe_status run_combine_fp8(const Dims& d, const uint8_t* y_q, const float* y_scale,
+                           const int32_t* dest_row, const float* topk_w, moe_bf16* y,
+                           cudaStream_t st) {
+  CombineArgs c;
+  c.T = d.T;
+  c.H = d.H;
+  c.k = d.k;
+  c.y_perm = nullptr;
+  c.dest_row = dest_row;
+  c.topk_w = topk_w;
+  c.y = y;
+  MOE_CUDA(launch_combine_fp8(c, y_q, y_scale, num_sms(), st));
   return MOE_OK;
 }
 
@@ -694,11 +718,16 @@ static moe_status layer_fwd(const moe_shape* s, const moe_bf16* x, const moe_bf1
     uint8_t* xq = reinterpret_cast<uint8_t*>(w.x_perm);
     MOE_TRY(run_gather_fp8(d, x, idx, off, dest, w.src_token, xq, w.x_scale, status, w, st));
     if (!mark(3)) return MOE_ERR_CUDA;
-    MOE_TRY(run_ffn_fp8(d, xq, w.x_scale, off, q->W1q, q->w1s, q->W2q, q->w2s, w.act, w.y_perm,
-                        status, w, st, events ? events + 4 : nullptr));
+    MOE_TRY(run_ffn_fp8(d, xq, w.x_scale, off, q->W1q, q->w1s, q->W2q, q->w2s, w.act, nullptr,
+                        status, w, st, events ? events + 4 : nullptr,
+                        reinterpret_cast<uint8_t*>(w.y_perm), w.y_scale));
   }
   if (!mark(5)) return MOE_ERR_CUDA;
-  MOE_TRY(run_combine(d, w.y_perm, dest, wts, y, st));
+  if (q == nullptr)
+    MOE_TRY(run_combine(d, w.y_perm, dest, wts, y, st));
+  else
+    MOE_TRY(run_combine_fp8(d, reinterpret_cast<const uint8_t*>(w.y_perm), w.y_scale, dest, wts,
+                            y, st));
   if (!mark(6)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -827,8 +856,8 @@ moe_status moe_permute_fp8(const moe_shape* s, const moe_bf16* x, const int32_t*
 moe_status moe_expert_ffn_fp8(const moe_shape* s, const uint8_t* x_q, const float* x_scale,
                               const int32_t* offsets, const uint8_t* W1q, const float* w1_scale,
                               const uint8_t* W2q, const float* w2_scale, moe_bf16* act,
-                              moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
-                              void* stream) {
+                              moe_bf16* y_perm, uint8_t* y_q, float* y_scale,
+                              uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_shape(s));
   MOE_REQUIRE(x_q);
   MOE_REQUIRE(x_scale);
@@ -838,14 +867,34 @@ moe_status moe_expert_ffn_fp8(const moe_shape* s, const uint8_t* x_q, const floa
   MOE_REQUIRE(W2q);
   MOE_REQUIRE(w2_scale);
   MOE_REQUIRE(act);
-  MOE_REQUIRE(y_perm);
+  // the expert outputs: bf16 y_perm, or e4m3 y_q with its block scales
+  if (y_perm != nullptr && y_q != nullptr) return MOE_ERR_UNSUPPORTED;
+  if (y_q != nullptr) {
+    MOE_REQUIRE(y_q);
+    MOE_REQUIRE(y_scale);
+  } else {
+    MOE_REQUIRE(y_perm);
+  }
   MOE_OPTIONAL(dev_status);
   const Dims d = dims_of(s);
   Ws w;
   MOE_TRY(carve(s, d, ws, ws_bytes, &w, true));
   uint32_t* status = dev_status ? dev_status : w.status;
   return run_ffn_fp8(d, x_q, x_scale, offsets, W1q, w1_scale, W2q, w2_scale, act, y_perm, status,
-                     w, static_cast<cudaStream_t>(stream), nullptr);
+                     w, static_cast<cudaStream_t>(stream), nullptr, y_q, y_scale);
+}
+
+moe_status moe_combine_fp8(const moe_shape* s, const uint8_t* y_q, const float* y_scale,
+                           const int32_t* dest_row, const float* topk_w, moe_bf16* y,
+                           void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(y_q);
+  MOE_REQUIRE(y_scale);
+  MOE_REQUIRE(dest_row);
+  MOE_REQUIRE(topk_w);
+  MOE_REQUIRE(y);
+  const Dims d = dims_of(s);
+  return run_combine_fp8(d, y_q, y_scale, dest_row, topk_w, y, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, const moe_bf16* gate,

@@ -8,6 +8,7 @@
 // every operation in fp32; a zero row has q = 0 and scale = 0. A value is
 // then q * scale, and a GEMM of two quantised operands is the fp32
 // accumulation of q products times the row scale times the column scale.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -195,7 +196,120 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(GatherArgs a, uint8_t* 
   }
 }
 
+// ----------------------------------------------------------- combine ----
+
+// 16 e4m3 values (one uint4) -> fp32, through the exact e4m3 -> f16 convert.
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4 v, float (&f)[16]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+          static_cast<__nv_fp8x2_storage_t>((w[q] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&r));
+      f[4 * q + 2 * h] = t.x;
+      f[4 * q + 2 * h + 1] = t.y;
+    }
+  }
+}
+
+// The FP8 combine: y[t] = bf16(sum over kept slots, ascending j, of w[t,j] *
+// q[dest, c] * scale[dest, c / 128]); one warp per token, 16 columns per
+// lane and vector, every slot's loads issued before any is used.
+template <int KMAX, int U>
+__global__ void __launch_bounds__(256, 2) combine_fp8_kernel(CombineArgs a,
+                                                             const uint8_t* __restrict__ y_q,
+                                                             const float* __restrict__ y_scale) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int nvec = a.H >> 4;
+  const int nblk = (a.H + 127) >> 7;
+  const uint4* __restrict__ yv = reinterpret_cast<const uint4*>(y_q);
+  uint4* __restrict__ ov = reinterpret_cast<uint4*>(a.y);
+  const int rows = a.T * a.k;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < a.T; t += warps) {
+    int dl = -1;
+    float wl = 0.f;
+    if (lane < a.k) {
+      dl = a.dest_row[static_cast<size_t>(t) * a.k + lane];
+      wl = a.topk_w[static_cast<size_t>(t) * a.k + lane];
+      if (dl < 0 || dl >= rows) dl = -1;  // only rows of the buffer are read
+    }
+    int d[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      d[j] = __shfl_sync(0xffffffffu, dl, j);
+      w[j] = __shfl_sync(0xffffffffu, wl, j);
+      if (j >= a.k) d[j] = -1;
+    }
+    for (int b = 0; b < nvec; b += 32 * U) {
+      uint4 v[KMAX][U];
+      float sc[KMAX][U];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = b + 32 * u + lane;
+          const bool ok = d[j] >= 0 && i < nvec;
+          v[j][u] = ok ? __ldg(yv + static_cast<size_t>(d[j]) * nvec + i) : make_uint4(0, 0, 0, 0);
+          sc[j][u] = ok ? __ldg(y_scale + static_cast<size_t>(d[j]) * nblk + (i >> 3)) : 0.f;
+        }
+      float acc[U][16];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[u][q] = 0.f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (d[j] >= 0) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            float f[16];
+            e4m3x16_to_f32(v[j][u], f);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc[u][q] = fmaf(w[j], f[q] * sc[j][u], acc[u][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = b + 32 * u + lane;
+        if (i < nvec) {
+          uint4 o0, o1;
+          o0.x = pack_bf16x2(acc[u][0], acc[u][1]);
+          o0.y = pack_bf16x2(acc[u][2], acc[u][3]);
+          o0.z = pack_bf16x2(acc[u][4], acc[u][5]);
+          o0.w = pack_bf16x2(acc[u][6], acc[u][7]);
+          o1.x = pack_bf16x2(acc[u][8], acc[u][9]);
+          o1.y = pack_bf16x2(acc[u][10], acc[u][11]);
+          o1.z = pack_bf16x2(acc[u][12], acc[u][13]);
+          o1.w = pack_bf16x2(acc[u][14], acc[u][15]);
+          uint4* dst = ov + static_cast<size_t>(t) * (a.H >> 3) + 2 * i;
+          dst[0] = o0;
+          dst[1] = o1;
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_fp8(const CombineArgs& a, const uint8_t* y_q, const float* y_scale,
+                               int num_sms, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  int grid = (a.T + 7) / 8;
+  if (grid > num_sms * 8) grid = num_sms * 8;
+  if (a.k <= 2)
+    combine_fp8_kernel<2, 2><<<grid, 256, 0, st>>>(a, y_q, y_scale);
+  else if (a.k <= 4)
+    combine_fp8_kernel<4, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
+  else
+    combine_fp8_kernel<8, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, int E, int K,
                                     int N, cudaStream_t st) {

@@ -17,6 +17,8 @@
 // taking half of the 256 columns. Stage and accumulator barriers are
 // released to both CTAs by multicast commits; the leader waits for both
 // epilogues before reusing an accumulator.
+#include <cuda_fp8.h>
+
 #include "moe_internal.h"
 #include "moe_ptx.cuh"
 
@@ -71,7 +73,11 @@ __device__ __forceinline__ float gelu_tanh_f(float u) {
 // stage row), the UMMA is kind::f8f6f4 and the epilogue multiplies by the
 // row scale of A and the column scale of B. Otherwise bf16 A (K-major) and
 // bf16 B (MN-major), 64 elements per stage row.
-template <bool kFp8>
+// kQOut (with kFp8): the output is e4m3 with one scale per 128-column block
+// of a row - exactly the columns one epilogue warp holds - formed from the
+// bf16-rounded values: a first pass over the warp's TMEM chunks finds the
+// block maximum, a second one converts and stores.
+template <bool kFp8, bool kQOut>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, GemmArgs p) {
@@ -311,44 +317,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                               static_cast<uint32_t>(acc * kBN + half * (kBN / 2));
       // two register sets: the next chunk's TMEM load overlaps this chunk's math
       uint32_t ra[32], rb[32];
-      if (n_chunks > 0) {
-        tmem_ld_32x32b_x32(t_base, ra);
-        tmem_ld_wait();
-      }
+      if constexpr (kQOut) {
+        const int n_it = 2 * n_chunks;  // pass 1: block maximum; pass 2: convert
+        float bmax = 0.f, inv = 0.f;
+        if (n_it > 0) {
+          tmem_ld_32x32b_x32(t_base, ra);
+          tmem_ld_wait();
+        }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        if (cc < n_chunks) {
-          uint32_t(&r)[32] = (cc & 1) ? rb : ra;
-          uint32_t(&nx)[32] = (cc & 1) ? ra : rb;
-          if (cc + 1 < n_chunks) tmem_ld_32x32b_x32(t_base + 32u * (cc + 1), nx);
-          if (valid) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float v0 = __uint_as_float(r[2 * i]);
-              float v1 = __uint_as_float(r[2 * i + 1]);
-              if constexpr (kFp8) {
-                v0 = v0 * rs * wscale[32 * cc + 2 * i];
-                v1 = v1 * rs * wscale[32 * cc + 2 * i + 1];
-              }
-              if (p.gelu) {
-                v0 = gelu_tanh_f(v0);
-                v1 = gelu_tanh_f(v1);
-              }
-              if constexpr (kFp8) row_max = fmaxf(row_max, fmaxf(fabsf(v0), fabsf(v1)));
-              packed[i] = pack_bf16x2(v0, v1);
+        for (int it = 0; it < 8; ++it) {
+          if (it < n_it) {
+            uint32_t(&r)[32] = (it & 1) ? rb : ra;
+            uint32_t(&nx)[32] = (it & 1) ? ra : rb;
+            const int cc = it < n_chunks ? it : it - n_chunks;
+            if (it + 1 < n_it) {
+              const int nc = it + 1 < n_chunks ? it + 1 : it + 1 - n_chunks;
+              tmem_ld_32x32b_x32(t_base + 32u * nc, nx);
             }
-            // outputs are read once, by the next kernel: stream them past L2
-            uint4* dst = reinterpret_cast<uint4*>(drow + col0 + 32 * cc);
+            if (it == n_chunks) inv = bmax > 0.f ? 448.0f / bmax : 0.f;
+            if (valid) {
+              uint32_t q4[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1],
-                                                  packed[4 * i + 2], packed[4 * i + 3]));
+              for (int i = 0; i < 16; ++i) {
+                float v0 = __uint_as_float(r[2 * i]) * rs * wscale[32 * cc + 2 * i];
+                float v1 = __uint_as_float(r[2 * i + 1]) * rs * wscale[32 * cc + 2 * i + 1];
+                if (p.gelu) {
+                  v0 = gelu_tanh_f(v0);
+                  v1 = gelu_tanh_f(v1);
+                }
+                const uint32_t b2 = pack_bf16x2(v0, v1);  // the bf16 outputs
+                if (it < n_chunks) {
+                  bmax = fmaxf(bmax, fmaxf(fabsf(bf16_lo(b2)), fabsf(bf16_hi(b2))));
+                } else {
+                  const uint32_t h = __nv_cvt_float2_to_fp8x2(
+                      make_float2(bf16_lo(b2) * inv, bf16_hi(b2) * inv), __NV_SATFINITE, __NV_E4M3);
+                  if (i & 1) q4[i >> 1] |= h << 16;
+                  else q4[i >> 1] = h;
+                }
+              }
+              if (it >= n_chunks) {
+                uint4* dst = reinterpret_cast<uint4*>(p.Dq + static_cast<size_t>(row) * p.N + col0 +
+                                                      32 * cc);
+                st_global_cs_v4(dst, make_uint4(q4[0], q4[1], q4[2], q4[3]));
+                st_global_cs_v4(dst + 1, make_uint4(q4[4], q4[5], q4[6], q4[7]));
+              }
+            }
+            if (it + 1 < n_it) tmem_ld_wait();
           }
-          if (cc + 1 < n_chunks) tmem_ld_wait();
+        }
+        if (valid && n_chunks > 0)
+          p.d_scale[static_cast<size_t>(row) * ((p.N + 127) / 128) + col0 / 128] = bmax / 448.0f;
+      } else {
+        if (n_chunks > 0) {
+          tmem_ld_32x32b_x32(t_base, ra);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (cc < n_chunks) {
+            uint32_t(&r)[32] = (cc & 1) ? rb : ra;
+            uint32_t(&nx)[32] = (cc & 1) ? ra : rb;
+            if (cc + 1 < n_chunks) tmem_ld_32x32b_x32(t_base + 32u * (cc + 1), nx);
+            if (valid) {
+              uint32_t packed[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float v0 = __uint_as_float(r[2 * i]);
+                float v1 = __uint_as_float(r[2 * i + 1]);
+                if constexpr (kFp8) {
+                  v0 = v0 * rs * wscale[32 * cc + 2 * i];
+                  v1 = v1 * rs * wscale[32 * cc + 2 * i + 1];
+                }
+                if (p.gelu) {
+                  v0 = gelu_tanh_f(v0);
+                  v1 = gelu_tanh_f(v1);
+                }
+                if constexpr (kFp8) row_max = fmaxf(row_max, fmaxf(fabsf(v0), fabsf(v1)));
+                packed[i] = pack_bf16x2(v0, v1);
+              }
+              // outputs are read once, by the next kernel: stream them past L2
+              uint4* dst = reinterpret_cast<uint4*>(drow + col0 + 32 * cc);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                st_global_cs_v4(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1],
+                                                    packed[4 * i + 2], packed[4 * i + 3]));
+            }
+            if (cc + 1 < n_chunks) tmem_ld_wait();
+          }
         }
       }
-      if constexpr (kFp8) {
+      if constexpr (kFp8 && !kQOut) {
         // bf16 rounding is monotonic, so the rounded maximum is the maximum
         // of the rounded (stored) values
         if (p.row_amax != nullptr && valid && n_chunks > 0)
@@ -378,7 +436,7 @@ size_t gemm_pair_smem_bytes(int E, int stages, bool fp8) {
          8 * (2 * stages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kQOut>
 cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
                         int num_sms, cudaStream_t st) {
   // the deepest ring that fits: every stage in flight hides TMA latency
@@ -392,7 +450,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   while (args.stages > 2 && gemm_pair_smem_bytes(a.E, args.stages, kFp8) > static_cast<size_t>(optin))
     --args.stages;
   const size_t smem = gemm_pair_smem_bytes(a.E, args.stages, kFp8);
-  err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8>,
+  err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8, kQOut>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -408,19 +466,20 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8>, tm_a, tm_b, args);
+  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8, kQOut>, tm_a, tm_b, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st) {
-  return launch_pair<false>(tm_a, tm_b, a, num_sms, st);
+  return launch_pair<false, false>(tm_a, tm_b, a, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                          const GemmArgs& a, int num_sms, cudaStream_t st) {
-  return launch_pair<true>(tm_a, tm_b, a, num_sms, st);
+  if (a.Dq != nullptr) return launch_pair<true, true>(tm_a, tm_b, a, num_sms, st);
+  return launch_pair<true, false>(tm_a, tm_b, a, num_sms, st);
 }
 
 }  // namespace moe

@@ -98,6 +98,8 @@ struct GemmArgs {
   const float* b_scale;    // FP8 mode: per-column scales of B [E, N]
   uint32_t* row_amax;      // FP8 mode, optional: max |bf16 output| per row, fp32 bits,
                            // combined with atomicMax (zeroed by the caller)
+  uint8_t* Dq;             // FP8 mode, optional: e4m3 output [rows, N] instead of D, with
+  float* d_scale;          //   one scale per (row, 128-column block): [rows, ceil(N/128)]
   int stages;              // CTA-pair kernel: pipeline depth (set by its launcher)
   uint32_t* dev_status;
   uint64_t timeout_ns;
@@ -122,8 +124,11 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st);
 size_t gemm_pair_smem_bytes(int E, int stages, bool fp8);
+// FP8 operands; writes D (bf16), or Dq + d_scale when a.Dq is set
 cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                          const GemmArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_combine_fp8(const CombineArgs& a, const uint8_t* y_q, const float* y_scale,
+                               int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, int E, int K,
                                     int N, cudaStream_t st);
 cudaError_t launch_row_quant(const uint16_t* src, const uint32_t* amax, uint8_t* dst,
