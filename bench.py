@@ -38,7 +38,8 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) per grouped-GEMM launch, averaged over GEMM1 and
 # GEMM2, from the ncu capture summarised in profiles/ (null until captured
 # for the current kernel).
-TRAFFIC = {"large_expert": 15.64e9}
+TRAFFIC = {"large_expert": 12.29e9}
+TRAFFIC_FP8 = {"large_expert": 4.60e9}
 
 
 def peaks():
@@ -302,7 +303,7 @@ def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2
                 "unit": "TFLOP/s", "frac": round(gemm_tf / peak, 4),
                 "peak_kind": kind,
                 "frac_of_burst": round(gemm_tf / burst, 4),
-                "traffic": None if args.fp8 else TRAFFIC.get(w.name)}
+                "traffic": (TRAFFIC_FP8 if args.fp8 else TRAFFIC).get(w.name)}
     tokens = T * world
     line = {
         "metric": METRIC, "value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s",
