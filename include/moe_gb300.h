@@ -154,8 +154,9 @@ MOE_API moe_status moe_route_gumbel(const moe_shape* s, const moe_bf16* x, const
  *        dest_row [T,k] = offsets[e] + position, or -1 if dropped;
  *        src_token [T*k] (row -> token, rows < offsets[E]);
  *        x_perm [T*k,H] bf16 (row dest_row[t,j] = x[t]).
- * kept_counts, src_token may be NULL. Bad or repeated indices set
- * MOE_DEV_BAD_INDEX / MOE_DEV_DUP_INDEX and that slot is dropped. */
+ * kept_counts, src_token may be NULL; x_perm may be NULL when src_token is
+ * given (the permutation only, for moe_expert_ffn_gathered). Bad or repeated
+ * indices set MOE_DEV_BAD_INDEX / MOE_DEV_DUP_INDEX and that slot is dropped. */
 MOE_API moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,
                        int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
                        int32_t* src_token, moe_bf16* x_perm, uint32_t* dev_status,
@@ -172,6 +173,22 @@ MOE_API moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, co
                           const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
                           moe_bf16* y_perm, uint32_t* dev_status, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* moe_expert_ffn with the dispatch's row copy fused into GEMM1's operand
+ * load: row r of GEMM1's A is x[src_token[r]], fetched by TMA row gathers,
+ * so the permuted copy x_perm is neither written nor read. The pages print
+ * no such step: it removes, on one GPU, the round trip of the dispatch bytes
+ * (MoE comm bottleneck section 2.1). Same act / y_perm as moe_expert_ffn on
+ * x_perm = x[src_token]. src_token [T*k] from moe_permute (rows <
+ * offsets[E]); entries outside [0, T) read row 0 or T-1. It saves the
+ * T*k*H*2-byte x_perm buffer and its traffic but runs GEMM1 about 3x slower
+ * on GB300 (the TMA moves the A operand as 32 four-row gathers per stage
+ * instead of one tile), so moe_layer_fwd keeps the permuted copy. */
+MOE_API moe_status moe_expert_ffn_gathered(const moe_shape* s, const moe_bf16* x,
+                                   const int32_t* src_token, const int32_t* offsets,
+                                   const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
+                                   moe_bf16* y_perm, uint32_t* dev_status, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /* Combine: weighted sum of each token's kept expert rows, back at the
  * token's position (MoE comm bottleneck, section 1.1, the combine step).

@@ -144,6 +144,11 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert lib.moe_route_logits(ctypes.byref(s), f, f, f, None, None, None, None, f,
                                 ws_need - 1, None) == 4
     assert lib.moe_permute(ctypes.byref(s), f, f, None, f, f, None, f, None, None, 0, None) == 1
+    # no x_perm and no src_token: nothing to write the permutation to
+    assert lib.moe_permute(ctypes.byref(s), f, f, None, f, f, None, None, None, f, ws_need,
+                           None) == 1
+    assert lib.moe_expert_ffn_gathered(ctypes.byref(s), f, None, f, f, f, f, f, None, f, ws_need,
+                                       None) == 1
     # bad shapes
     bad = _shape(E=300)
     assert lib.moe_expert_ffn(ctypes.byref(bad), f, f, f, f, f, f, f, None, 0, None) == 3

@@ -304,6 +304,71 @@ def test_expert_ffn_against_oracle(E, H, h, counts):
     assert_ffn_close(np64(yp[:N]), O.expert_ffn(x64, off, W1n, W2n), "y_perm (oracle chain)")
 
 
+@pytest.mark.parametrize("T,H,E,k,h,cf,skew", [
+    (300, 128, 5, 2, 192, 1.0, 1.0),         # small: ragged segments, drops
+    (1000, 256, 12, 3, 320, 0.8, 0.5),       # partial N tile, drops
+    (4096, 512, 8, 2, 256, 1.25, 0.0),       # >= 4096 rows: same kernel as moe_expert_ffn
+])
+def test_expert_ffn_gathered_against_oracle(T, H, E, k, h, cf, skew):
+    """GEMM1 reads x[src_token] by TMA row gathers: same results as the
+    oracle FFN on the permuted rows, and (same kernel) the same bits as
+    moe_expert_ffn on the permuted copy."""
+    gen = torch.Generator().manual_seed(T + E)
+    x = torch.randn((T, H), generator=gen).to(torch.bfloat16)
+    W1 = (torch.randn((E, H, h), generator=gen) / H ** 0.5).to(torch.bfloat16)
+    W2 = (torch.randn((E, h, H), generator=gen) / h ** 0.5).to(torch.bfloat16)
+    idx = W.make_topk_idx(T, E, k, skew=skew, seed=T)
+    d = O.dispatch_plan(idx.numpy(), E, O.capacity(T, E, k, cf))
+    N, A = int(d.offsets[-1]), T * k
+    src = torch.full((A,), 10 ** 8, dtype=torch.int32)   # rows past N: never read
+    src[:N] = torch.from_numpy(d.src_token[:N].astype(np.int32))
+    off = torch.from_numpy(d.offsets.astype(np.int32))
+    s = _shape(T, H, E, k, h, cf)
+    act = _zeros((A, h), torch.bfloat16)
+    yp = _zeros((A, H), torch.bfloat16)
+    st = _status()
+    moe.moe_expert_ffn_gathered(s, x.to(DEV), src.to(DEV), off.to(DEV), W1.to(DEV), W2.to(DEV),
+                                act, yp, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    xp64 = np64(x)[d.src_token[:N]]
+    W1n, W2n = np64(W1), np64(W2)
+    ref_act = np.zeros((N, h))
+    for e in range(E):
+        a, b = int(d.offsets[e]), int(d.offsets[e + 1])
+        if b > a:
+            ref_act[a:b] = O.bf16_round(O.gelu_tanh(xp64[a:b] @ W1n[e]))
+    assert_ffn_close(np64(act[:N]), ref_act, "act (gathered)")
+    assert_ffn_close(np64(yp[:N]), O.expert_ffn(xp64, d.offsets, W1n, W2n), "y_perm (gathered)")
+    if A >= 4096:
+        xp = torch.zeros((A, H), dtype=torch.bfloat16)
+        xp[:N] = x[torch.from_numpy(d.src_token[:N].astype(np.int64))]
+        act2, yp2, st2 = _ffn_gpu(s, xp, d.offsets.astype(np.int32), W1, W2)
+        assert st2 == 0
+        assert torch.equal(act2[:N], act[:N].cpu()) and torch.equal(yp2[:N], yp[:N].cpu())
+
+
+def test_permute_indices_only():
+    """moe_permute without x_perm writes the same permutation."""
+    T, H, E, k = 1000, 64, 12, 3
+    idx = W.make_topk_idx(T, E, k, skew=1.0, seed=2)
+    x = torch.randn((T, H)).to(torch.bfloat16)
+    s = _shape(T, H, E, k, 64, 0.9)
+    ws = moe.Workspace(s)
+    outs = []
+    for with_rows in (True, False):
+        off = _zeros(E + 1, torch.int32)
+        dest = _zeros((T, k), torch.int32)
+        src = _zeros(T * k, torch.int32)
+        xp = _zeros((T * k, H), torch.bfloat16) if with_rows else None
+        moe.moe_permute(s, x.to(DEV), idx.to(DEV), None, off, dest, src, xp, ws=ws)
+        torch.cuda.synchronize()
+        n = int(off[-1].item())
+        outs.append((off.cpu(), dest.cpu(), src[:n].cpu()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 # ============================================================ combine ====
 
 @pytest.mark.parametrize("T,H,k,drop", [(512, 256, 2, 0.0), (1000, 512, 3, 0.3), (77, 64, 8, 0.5),

@@ -23,7 +23,7 @@ __all__ = [
     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
     "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
     "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
-    "moe_layer_fwd_fp8", "moe_combine_fp8", "Fp8Weights",
+    "moe_layer_fwd_fp8", "moe_combine_fp8", "Fp8Weights", "moe_expert_ffn_gathered",
     "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "mo
                     "moe_host_workspace_size", "moe_layer_fwd_host", "moe_route_gumbel",
                     "moe_layer_fwd_gumbel", "moe_workspace_size_fp8", "moe_quantize_weights_fp8",
                     "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8",
-                    "moe_combine_fp8"]
+                    "moe_combine_fp8", "moe_expert_ffn_gathered"]
 
 
 class MoeError(RuntimeError):
@@ -106,6 +106,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_permute_fp8.argtypes = [S] + [_P] * 10 + [ctypes.c_size_t, _P]
     lib.moe_expert_ffn_fp8.restype = ctypes.c_int
     lib.moe_expert_ffn_fp8.argtypes = [S] + [_P] * 13 + [ctypes.c_size_t, _P]
+    lib.moe_expert_ffn_gathered.restype = ctypes.c_int
+    lib.moe_expert_ffn_gathered.argtypes = [S] + [_P] * 9 + [ctypes.c_size_t, _P]
     lib.moe_combine_fp8.restype = ctypes.c_int
     lib.moe_combine_fp8.argtypes = [S] + [_P] * 6
     lib.moe_layer_fwd_fp8.restype = ctypes.c_int
@@ -251,6 +253,20 @@ def moe_expert_ffn(shape, x_perm, offsets, W1, W2, act, y_perm, dev_status=None,
         _ptr(W1, torch.bfloat16, "W1"), _ptr(W2, torch.bfloat16, "W2"),
         _ptr(act, torch.bfloat16, "act"), _ptr(y_perm, torch.bfloat16, "y_perm"),
         _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+
+
+def moe_expert_ffn_gathered(shape, x, src_token, offsets, W1, W2, act, y_perm, dev_status=None,
+                            ws: Workspace | None = None, stream=None):
+    """moe_expert_ffn on x[src_token] without the permuted copy: GEMM1
+    gathers its A rows from x by TMA."""
+    s = _shape(shape)
+    wp, wn = _ws(ws, s)
+    _check("moe_expert_ffn_gathered", load_library().moe_expert_ffn_gathered(
+        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(src_token, torch.int32, "src_token"),
+        _ptr(offsets, torch.int32, "offsets"), _ptr(W1, torch.bfloat16, "W1"),
+        _ptr(W2, torch.bfloat16, "W2"), _ptr(act, torch.bfloat16, "act"),
+        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        wp, wn, _stream(stream)))
 
 
 def moe_combine(shape, y_perm, dest_row, topk_w, y, stream=None):

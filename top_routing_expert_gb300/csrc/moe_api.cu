@@ -370,11 +370,18 @@ moe_status run_gather_fp8(const Dims& d, const moe_bf16* x, const int32_t* idx,
   return MOE_OK;
 }
 
+// With a_rows, A row r is row a_rows[r] of A (a tensor of a_src_rows rows),
+// gathered by the CTA-pair kernel's TMA (box one row high).
 moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const int32_t* offsets,
-                    int K, int N, moe_bf16* D, int gelu, uint32_t* status, cudaStream_t st) {
+                    int K, int N, moe_bf16* D, int gelu, uint32_t* status, cudaStream_t st,
+                    const int32_t* a_rows = nullptr, int a_src_rows = 0) {
   if (d.A == 0) return MOE_OK;
   CUtensorMap tm_a, tm_b;
-  if (!tmap_bf16_2d(&tm_a, A, K, d.A, kBlockK, 128)) return MOE_ERR_CUDA;
+  if (a_rows != nullptr) {
+    if (!tmap_bf16_2d(&tm_a, A, K, a_src_rows, kBlockK, 1)) return MOE_ERR_CUDA;
+  } else if (!tmap_bf16_2d(&tm_a, A, K, d.A, kBlockK, 128)) {
+    return MOE_ERR_CUDA;
+  }
   if (!tmap_bf16_2d(&tm_b, W, N, static_cast<uint64_t>(d.E) * K, 64, kBlockK)) return MOE_ERR_CUDA;
   GemmArgs g;
   g.offsets = offsets;
@@ -389,9 +396,11 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.row_amax = nullptr;
   g.Dq = nullptr;
   g.d_scale = nullptr;
+  g.a_rows = a_rows;
+  g.a_src_rows = a_src_rows;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
-  if (d.A >= kPairGemmMinRows)
+  if (d.A >= kPairGemmMinRows || a_rows != nullptr)
     MOE_CUDA(launch_grouped_gemm_pair(tm_a, tm_b, g, num_sms(), st));
   else
     MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));
@@ -422,6 +431,8 @@ moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
   g.row_amax = row_amax;
   g.Dq = Dq;
   g.d_scale = d_scale;
+  g.a_rows = nullptr;
+  g.a_src_rows = 0;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   MOE_CUDA(launch_grouped_gemm_pair_fp8(tm_a, tm_b, g, num_sms(), st));
@@ -572,10 +583,11 @@ moe_status moe_permute(const moe_shape* s, const moe_bf16* x, const int32_t* top
   MOE_REQUIRE(topk_idx);
   MOE_REQUIRE(offsets);
   MOE_REQUIRE(dest_row);
-  MOE_REQUIRE(x_perm);
+  MOE_OPTIONAL(x_perm);  // NULL: the permutation only (for moe_expert_ffn_gathered)
   MOE_OPTIONAL(kept_counts);
   MOE_OPTIONAL(src_token);
   MOE_OPTIONAL(dev_status);
+  if (x_perm == nullptr && src_token == nullptr) return MOE_ERR_NULL;
   const Dims d = dims_of(s);
   Ws w;
   MOE_TRY(carve(s, d, ws, ws_bytes, &w));
@@ -623,6 +635,33 @@ moe_status moe_expert_ffn(const moe_shape* s, const moe_bf16* x_perm, const int3
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_TRY(run_gemm(d, x_perm, W1, offsets, d.H, d.h, act, 1, status, st));
+  MOE_TRY(run_gemm(d, act, W2, offsets, d.h, d.H, y_perm, 0, status, st));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_gathered(const moe_shape* s, const moe_bf16* x,
+                                   const int32_t* src_token, const int32_t* offsets,
+                                   const moe_bf16* W1, const moe_bf16* W2, moe_bf16* act,
+                                   moe_bf16* y_perm, uint32_t* dev_status, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(src_token);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(W1);
+  MOE_REQUIRE(W2);
+  MOE_REQUIRE(act);
+  MOE_REQUIRE(y_perm);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  uint32_t* status = dev_status;
+  if (status == nullptr) {
+    Ws w;
+    MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+    status = w.status;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(run_gemm(d, x, W1, offsets, d.H, d.h, act, 1, status, st, src_token, d.T));
   MOE_TRY(run_gemm(d, act, W2, offsets, d.h, d.H, y_perm, 0, status, st));
   return MOE_OK;
 }

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
     int d[kMaxTopK];
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) d[j] = __shfl_sync(0xffffffffu, dest, j);
+    if (pv == nullptr) continue;  // index-only dispatch: GEMM1 gathers the rows itself
 
     const uint4* src = xv + static_cast<size_t>(t) * nvec;
     for (int b = 0; b < nvec; b += 32 * U) {

@@ -73,11 +73,15 @@ __device__ __forceinline__ float gelu_tanh_f(float u) {
 // stage row), the UMMA is kind::f8f6f4 and the epilogue multiplies by the
 // row scale of A and the column scale of B. Otherwise bf16 A (K-major) and
 // bf16 B (MN-major), 64 elements per stage row.
+// kGather (bf16): A row r is row a_rows[r] of the token matrix, fetched by
+// TMA tile::gather4 - the dispatch's permutation fused into the A load, so
+// no permuted copy of the tokens is written or read. The whole producer warp
+// issues: lane l gathers rows 4l..4l+3 of the CTA's 128-row tile.
 // kQOut (with kFp8): the output is e4m3 with one scale per 128-column block
 // of a row - exactly the columns one epilogue warp holds - formed from the
 // bf16-rounded values: a first pass over the warp's TMEM chunks finds the
 // block maximum, a second one converts and stores.
-template <bool kFp8, bool kQOut>
+template <bool kFp8, bool kQOut, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, GemmArgs p) {
@@ -163,8 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, p.dev_status, p.timeout_ns};
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer ----
+    // lanes 1-31 leave at once unless they gather (they must not fall
+    // through to the epilogue branch below)
+    if (kGather || lane == 0) {
+      // ------------------------------------------------------ TMA producer ----
+      // lane 0 waits, arms the barrier and loads B (and A when not gathered);
+      // with kGather every lane of the warp also gathers four A rows
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -174,26 +182,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
         const int b_row = c.e * p.K;
         const int b_col = c.n0 + static_cast<int>(rank) * (kBN / 2);
+        int gr[4] = {0, 0, 0, 0};
+        if constexpr (kGather) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = c.row0 + 4 * lane + q;
+            int t = r < c.row_end ? p.a_rows[r] : 0;  // rows past the segment: any valid row
+            gr[q] = t < 0 ? 0 : (t >= p.a_src_rows ? p.a_src_rows - 1 : t);
+          }
+        }
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+          bool ok = true;
+          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, wc);
+          if constexpr (kGather) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
             aborted = true;
             break;
           }
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
-          // A rows are reused by every n-tile of the group: keep them in L2
-          tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
-          if constexpr (kFp8) {
-            // B^T [E*N, K] e4m3: this CTA's 128 output columns as K-major rows
-            tma_load_2d_pair(sb, &tm_b, bar, kb * kKE, c.e * p.N + b_col);
-          } else {
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            // A rows are reused by every n-tile of the group: keep them in L2
+            if constexpr (!kGather) tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
+            if constexpr (kFp8) {
+              // B^T [E*N, K] e4m3: this CTA's 128 output columns as K-major rows
+              tma_load_2d_pair(sb, &tm_b, bar, kb * kKE, c.e * p.N + b_col);
+            } else {
 #pragma unroll
-            for (int cb = 0; cb < kBN / 2 / 64; ++cb)
-              tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
-                               b_row + kb * kBlockK);
+              for (int cb = 0; cb < kBN / 2 / 64; ++cb)
+                tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
+                                 b_row + kb * kBlockK);
+            }
           }
+          if constexpr (kGather)
+            tma_gather4_pair(sa + 512 * lane, &tm_a, bar, kb * kKE, gr[0], gr[1], gr[2], gr[3]);
           ++issued;
           if (++stage == nst) {
             stage = 0;
@@ -201,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (aborted) {
+      if (aborted && lane == 0) {
         if (leader) {
           // let the last loads issued land before the CTA exits (the leader's
           // barriers count both CTAs' bytes)
@@ -436,7 +460,7 @@ size_t gemm_pair_smem_bytes(int E, int stages, bool fp8) {
          8 * (2 * stages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
-template <bool kFp8, bool kQOut>
+template <bool kFp8, bool kQOut, bool kGather>
 cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
                         int num_sms, cudaStream_t st) {
   // the deepest ring that fits: every stage in flight hides TMA latency
@@ -450,7 +474,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   while (args.stages > 2 && gemm_pair_smem_bytes(a.E, args.stages, kFp8) > static_cast<size_t>(optin))
     --args.stages;
   const size_t smem = gemm_pair_smem_bytes(a.E, args.stages, kFp8);
-  err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8, kQOut>,
+  err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8, kQOut, kGather>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -466,20 +490,22 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8, kQOut>, tm_a, tm_b, args);
+  err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8, kQOut, kGather>, tm_a, tm_b,
+                           args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st) {
-  return launch_pair<false, false>(tm_a, tm_b, a, num_sms, st);
+  if (a.a_rows != nullptr) return launch_pair<false, false, true>(tm_a, tm_b, a, num_sms, st);
+  return launch_pair<false, false, false>(tm_a, tm_b, a, num_sms, st);
 }
 
 cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                          const GemmArgs& a, int num_sms, cudaStream_t st) {
-  if (a.Dq != nullptr) return launch_pair<true, true>(tm_a, tm_b, a, num_sms, st);
-  return launch_pair<true, false>(tm_a, tm_b, a, num_sms, st);
+  if (a.Dq != nullptr) return launch_pair<true, true, false>(tm_a, tm_b, a, num_sms, st);
+  return launch_pair<true, false, false>(tm_a, tm_b, a, num_sms, st);
 }
 
 }  // namespace moe

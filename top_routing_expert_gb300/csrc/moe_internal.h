@@ -100,6 +100,8 @@ struct GemmArgs {
                            // combined with atomicMax (zeroed by the caller)
   uint8_t* Dq;             // FP8 mode, optional: e4m3 output [rows, N] instead of D, with
   float* d_scale;          //   one scale per (row, 128-column block): [rows, ceil(N/128)]
+  const int32_t* a_rows;   // optional: A row r is row a_rows[r] of the A tensor (a gather,
+  int a_src_rows;          //   by TMA, from a tensor of a_src_rows rows); CTA-pair kernel
   int stages;              // CTA-pair kernel: pipeline depth (set by its launcher)
   uint32_t* dev_status;
   uint64_t timeout_ns;

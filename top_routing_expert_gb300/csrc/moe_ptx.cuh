@@ -277,6 +277,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Four rows of a 2-D tensor (row indices r0..r3, one 128-byte box row each,
+// from column c0) into consecutive 128-byte rows at smem_dst; the map's box
+// is one row high. Transaction bytes counted as in tma_load_2d_pair.
+__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t mbar_cluster_addr, int32_t c0,
+                                                 int32_t r0, int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // Collective over one warp of each CTA of the pair.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
