@@ -222,12 +222,44 @@ def run_ours(args, rank, world, local_rank):
     # the end-to-end leg times the inference layer; skipped for the training router
     e2e = None if (args.no_e2e or args.gumbel is not None or args.fp8) else \
         run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
+    dense = None if (args.fp8 or args.gumbel is not None) else \
+        run_dense_ffn(args, moe, w, d, stream, dev, flush is not None)
     if rank != 0:
         return None
     l2 = (f"L2 flushed between steps ({2 * L2_BYTES >> 20} MB write); steps timed by their own events"
           if flush is not None else
           f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB re-read per step); no flush")
-    return report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2)
+    return report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2, dense)
+
+
+def run_dense_ffn(args, moe, w, d, stream, dev, flush_l2):
+    """The secondary metric of the module notes' benchmark protocol (section
+    5.3): the MoE layer's time over that of one dense FFN of width h on the
+    same T tokens, run by the same grouped-GEMM kernels with E = 1 (expert 0's
+    weights, every token kept)."""
+    T, H, h = w.T, w.H, w.h
+    s1 = moe.MoeShape.make(T, H, 1, 1, h, 1.0)
+    ws1 = moe.Workspace(s1, device=dev)
+    off = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    W1 = d["W1"][:1].contiguous()
+    W2 = d["W2"][:1].contiguous()
+    act = torch.empty((T, h), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush_l2 else None
+    n = max(3, min(args.steps, 30))
+    for _ in range(3):
+        moe.moe_expert_ffn(s1, d["x"], off, W1, W2, act, yd, ws=ws1, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda.synchronize(dev)
+    for i in range(n):
+        if flush is not None:
+            flush.fill_(float(i))
+        ev[i][0].record(stream)
+        moe.moe_expert_ffn(s1, d["x"], off, W1, W2, act, yd, ws=ws1, stream=stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / n
 
 
 def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
@@ -264,7 +296,7 @@ def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
     return {"ms": e2e_ms, "h2d": T * H * 2, "d2h": T * H * 2 + 4}
 
 
-def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2):
+def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2, dense=None):
     T, k = w.T, w.k
     pk = peaks()
     work = algorithmic_work(w, n_kept, any_kept, fp8=args.fp8)
@@ -329,6 +361,11 @@ def report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2
         "routing": {"kept_rows": n_kept, "assignments": T * k, "dropped": T * k - n_kept,
                     "dev_status": st},
     }
+    if dense is not None:
+        line["moe_vs_dense_ffn"] = {
+            "dense_ffn_ms": round(dense, 4), "ratio": round(ms / dense, 3),
+            "what": "layer time / one dense FFN (h) over the same T tokens, same kernels, E=1",
+            "ideal_from_flops": round(n_kept / T, 3)}
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(OracleInputs(w, inp, fp8=args.fp8), args.cpu_tokens)
     return line

@@ -100,27 +100,52 @@ constexpr int kChunk = 8;
 // Router scores of the thread's row from TMEM (GEMM path): the logits plus
 // the bias, and for the training router (module notes, section 3.1) plus
 // Gumbel noise g = -log(-log(u + 1e-9) + 1e-9) from caller-drawn uniforms,
-// divided by the temperature.
+// divided by the temperature. The epilogue reads the scores in three passes:
+// load_first serves the first and, with noise, writes the finished scores
+// back over the accumulator (the uniforms are read and the logs taken once);
+// load_next serves the others. `noisy` is the same for every thread.
 struct TmemSource {
   uint32_t taddr;       // TMEM address of (this warp's lane quadrant, column 0)
   const float* bias_s;  // shared, zero past E
-  const float* u_row;   // this token's uniforms [E], or nullptr (no noise)
+  const float* u_row;   // this token's uniforms [E], or nullptr (no noise / no token)
   float temperature;
   int E;
-  __device__ __forceinline__ void load(int c, float (&v)[kChunk]) const {
+  bool noisy;           // the training router: scores are written back in pass 1
+  __device__ __forceinline__ void load_first(int c, float (&v)[kChunk]) const {
     uint32_t r[kChunk];
     tmem_ld_32x32b_x8(taddr + static_cast<uint32_t>(c), r);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]) + bias_s[c + i];
-    if (u_row != nullptr) {
+    if (noisy) {
+      if (u_row != nullptr) {
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        if (c + i < E) {
-          const float g = -logf(-logf(u_row[c + i] + 1e-9f) + 1e-9f);
-          v[i] = (v[i] + g) / temperature;
+        for (int i = 0; i < kChunk; ++i) {
+          if (c + i < E) {
+            const float g = -logf(-logf(u_row[c + i] + 1e-9f) + 1e-9f);
+            v[i] = (v[i] + g) / temperature;
+          }
         }
       }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) r[i] = __float_as_uint(v[i]);
+      tmem_st_32x32b_x8(taddr + static_cast<uint32_t>(c), r);
+    }
+  }
+  // after pass 1: the written-back scores are visible to this thread's loads
+  __device__ __forceinline__ void first_done() const {
+    if (noisy) tmem_st_wait();
+  }
+  __device__ __forceinline__ void load_next(int c, float (&v)[kChunk]) const {
+    uint32_t r[kChunk];
+    tmem_ld_32x32b_x8(taddr + static_cast<uint32_t>(c), r);
+    tmem_ld_wait();
+    if (noisy) {
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]) + bias_s[c + i];
     }
   }
 };
@@ -134,7 +159,9 @@ struct GlobalSource {
   const float* row;
   int E;
   bool valid;
-  __device__ __forceinline__ void load(int c, float (&v)[kChunk]) const {
+  __device__ __forceinline__ void load_first(int c, float (&v)[kChunk]) const { load_next(c, v); }
+  __device__ __forceinline__ void first_done() const {}
+  __device__ __forceinline__ void load_next(int c, float (&v)[kChunk]) const {
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const int e = c + i;
@@ -226,7 +253,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
 #pragma unroll 1
   for (int c = c0; c < cend; c += kChunk) {
     float v[kChunk];
-    src.load(c, v);
+    src.load_first(c, v);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const int e = c + i;
@@ -237,6 +264,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
       }
     }
   }
+  src.first_done();
   const int cbase = (r * npart + part) * KMAX;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
@@ -260,7 +288,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
 #pragma unroll 1
   for (int c = c0; c < cend; c += kChunk) {
     float v[kChunk];
-    src.load(c, v);
+    src.load_next(c, v);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i)
       if (c + i < E) s_loc += expf(v[i] - m);
@@ -291,7 +319,7 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
 #pragma unroll 1
   for (int c = c0; c < cend; c += kChunk) {
     float v[kChunk];
-    src.load(c, v);
+    src.load_next(c, v);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const int e = c + i;
@@ -484,7 +512,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   if (go) {
     const int t_row = tile * kTileTokens + 32 * (warp & 3) + lane;
     TmemSource src{tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16), sm.bias_s,
-                   noise_row(a, t_row), a.temperature, a.E};
+                   noise_row(a, t_row), a.temperature, a.E, a.noise_u != nullptr};
     // the pipeline stages are free now: they hold the epilogue scratch
     route_epilogue<KMAX>(src, a, tile, carve_epi(smem, npart, KMAX), sm.masks, sm.red, E32,
                          npart, cpt, CtaGroup{});
@@ -696,7 +724,8 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
       if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
       tc_fence_after();
       TmemSource src{tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * E32),
-                     bias_s, noise_row(a, tile * kTileTokens + 32 * q + lane), a.temperature, a.E};
+                     bias_s, noise_row(a, tile * kTileTokens + 32 * q + lane), a.temperature, a.E,
+                     a.noise_u != nullptr};
       route_epilogue<KMAX>(src, a, tile, es, masks, red, E32, L.npart, L.cpt, grp);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
