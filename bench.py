@@ -148,6 +148,7 @@ def run_ours(args, rank, world, local_rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    q = None
     if args.fp8:
         # weights are parameters: quantised once, before the timed region
         q = moe.Fp8Weights(d["W1"], d["W2"])
@@ -220,8 +221,8 @@ def run_ours(args, rank, world, local_rank):
     any_kept = int((dest >= 0).any(dim=1).sum().item())
 
     # the end-to-end leg times the inference layer; skipped for the training router
-    e2e = None if (args.no_e2e or args.gumbel is not None or args.fp8) else \
-        run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world)
+    e2e = None if (args.no_e2e or args.gumbel is not None) else \
+        run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world, q)
     dense = None if (args.fp8 or args.gumbel is not None) else \
         run_dense_ffn(args, moe, w, d, stream, dev, flush is not None)
     if rank != 0:
@@ -262,19 +263,21 @@ def run_dense_ffn(args, moe, w, d, stream, dev, flush_l2):
     return sum(a.elapsed_time(b) for a, b in ev) / n
 
 
-def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world):
+def run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world, q=None):
     """End to end through the public API with host buffers: every step is one
     micro-batch of moe_layer_fwd_host - its tokens copied in from pinned host
     memory, the layer, its output and aux copied back to the host - with the
     copies of neighbouring micro-batches overlapping the layer on three
     streams. Timed from before the first copy-in to after the last copy-out."""
     T, H = inp["x"].shape
-    pipe = moe.HostPipeline(s, device=dev)
+    pipe = moe.HostPipeline(s, device=dev, fp8=q is not None)
     x_host = inp["x"].pin_memory()
     y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     aux_host = torch.empty(max(args.steps, args.warmup), dtype=torch.float32).pin_memory()
 
     def run(n):
+        if q is not None:
+            return pipe.run([x_host] * n, [y_host] * n, d["gate"], d["bias"], q, None, aux_host)
         return pipe.run([x_host] * n, [y_host] * n, d["gate"], d["bias"], d["W1"], d["W2"],
                         aux_host)
 

@@ -329,6 +329,18 @@ MOE_API moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, cons
                              uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream,
                              void* const* events);
 
+/* moe_layer_fwd_host with the FP8 layer of moe_layer_fwd_fp8: the same
+ * three-stream micro-batch pipeline (bf16 tokens in, bf16 outputs out), with
+ * the quantised weights of moe_quantize_weights_fp8. ws must hold
+ * moe_host_workspace_size_fp8 bytes. Other arguments as moe_layer_fwd_host. */
+MOE_API moe_status moe_host_workspace_size_fp8(const moe_shape* s, size_t* bytes);
+MOE_API moe_status moe_layer_fwd_host_fp8(const moe_shape* s, int64_t n_micro,
+                                  const moe_bf16* const* x_host, moe_bf16* const* y_host,
+                                  float* aux_host, const moe_bf16* gate, const float* gate_bias,
+                                  const uint8_t* W1q, const float* w1_scale, const uint8_t* W2q,
+                                  const float* w2_scale, uint32_t* dev_status, void* ws,
+                                  size_t ws_bytes, void* const* streams, void* const* events);
+
 /* moe_permute for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it serves code that may not call
  * cudaMalloc or hold a workspace: a plugin inside a runtime that owns all

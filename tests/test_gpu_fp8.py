@@ -398,3 +398,31 @@ def test_combine_fp8_against_oracle(T, H, k, drop):
     assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + mag * 2.0 ** -20).all()
     assert np.mean(got == ref) > 0.98
     assert (got[(dest.numpy() < 0).all(axis=1)] == 0).all()
+
+
+def test_layer_fp8_host_pipeline_equals_device_layer():
+    """moe_layer_fwd_host_fp8 over three micro-batches (copies overlapped with
+    the FP8 layer on three streams) gives each micro-batch's
+    moe_layer_fwd_fp8 output bit for bit."""
+    w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="pipe8")
+    shape = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
+    base = W.make_inputs(w, seed=31)
+    xs = [W.make_inputs(w, seed=s, with_weights=False)["x"] for s in (32, 33, 34)]
+    gate, bias = base["gate"].to(DEV), base["bias"].to(DEV)
+    Q = moe.Fp8Weights(base["W1"].to(DEV), base["W2"].to(DEV))
+    pipe = moe.HostPipeline(shape, fp8=True)
+    x_host = [x.pin_memory() for x in xs]
+    y_host = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    aux_host = torch.zeros(len(xs), dtype=torch.float32).pin_memory()
+    status = _status()
+    moe.moe_layer_fwd_host_fp8(pipe, x_host, y_host, gate, bias, Q, aux_host, status).synchronize()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ws = moe.Workspace(shape, fp8=True)
+    for i, x in enumerate(xs):
+        y = _zeros((w.T, w.H), torch.bfloat16)
+        aux = _zeros(1, torch.float32)
+        moe.moe_layer_fwd_fp8(shape, x.to(DEV), gate, bias, Q, y, aux=aux, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y.cpu(), y_host[i]), i
+        assert float(aux.item()) == float(aux_host[i])

@@ -22,7 +22,7 @@ __all__ = [
     "abi_version", "moe_route", "moe_route_logits", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_layer_fwd", "moe_permute_noalloc", "moe_layer_fwd_host",
     "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
-    "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
+    "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_layer_fwd_host_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
     "moe_layer_fwd_fp8", "moe_combine_fp8", "Fp8Weights", "moe_expert_ffn_gathered",
     "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
@@ -36,7 +36,8 @@ EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "mo
                     "moe_host_workspace_size", "moe_layer_fwd_host", "moe_route_gumbel",
                     "moe_layer_fwd_gumbel", "moe_workspace_size_fp8", "moe_quantize_weights_fp8",
                     "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8",
-                    "moe_combine_fp8", "moe_expert_ffn_gathered"]
+                    "moe_combine_fp8", "moe_expert_ffn_gathered", "moe_host_workspace_size_fp8",
+                    "moe_layer_fwd_host_fp8"]
 
 
 class MoeError(RuntimeError):
@@ -98,6 +99,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_host_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_layer_fwd_host.restype = ctypes.c_int
     lib.moe_layer_fwd_host.argtypes = [S, ctypes.c_int64] + [_P] * 9 + [ctypes.c_size_t, _P, _P]
+    lib.moe_host_workspace_size_fp8.restype = ctypes.c_int
+    lib.moe_host_workspace_size_fp8.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_layer_fwd_host_fp8.restype = ctypes.c_int
+    lib.moe_layer_fwd_host_fp8.argtypes = [S, ctypes.c_int64] + [_P] * 11 + [ctypes.c_size_t, _P, _P]
     lib.moe_workspace_size_fp8.restype = ctypes.c_int
     lib.moe_workspace_size_fp8.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_quantize_weights_fp8.restype = ctypes.c_int
@@ -329,11 +334,19 @@ class HostPipeline:
     """Owns what moe_layer_fwd_host needs besides the weights: the device
     workspace, three CUDA streams (compute, copy-in, copy-out) and six
     events. Host token/output tensors should be pinned for the copies to
-    overlap the layer."""
+    overlap the layer. fp8=True sizes it for moe_layer_fwd_host_fp8 (run
+    with an Fp8Weights in place of W1 and W2 there)."""
 
-    def __init__(self, shape, device="cuda"):
+    def __init__(self, shape, device="cuda", fp8: bool = False):
         self.shape = _shape(shape)
-        self.nbytes = host_workspace_size(self.shape)
+        self.fp8 = fp8
+        if fp8:
+            n = ctypes.c_size_t(0)
+            _check("moe_host_workspace_size_fp8", load_library().moe_host_workspace_size_fp8(
+                ctypes.byref(self.shape), ctypes.byref(n)))
+            self.nbytes = n.value
+        else:
+            self.nbytes = host_workspace_size(self.shape)
         self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
         self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
         self.events = [torch.cuda.Event() for _ in range(6)]
@@ -356,6 +369,16 @@ class HostPipeline:
             aux = aux_host.data_ptr()
         st = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
         ev = (ctypes.c_void_p * 6)(*[e.cuda_event for e in self.events])
+        if self.fp8:
+            q = W1  # an Fp8Weights
+            _check("moe_layer_fwd_host_fp8", load_library().moe_layer_fwd_host_fp8(
+                ctypes.byref(self.shape), n, xs, ys, aux, _ptr(gate, torch.bfloat16, "gate"),
+                _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(q.W1q, torch.uint8, "W1q"),
+                _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
+                _ptr(q.w2_scale, torch.float32, "w2_scale"),
+                _ptr(dev_status, torch.int32, "dev_status"), self.buf.data_ptr(), self.nbytes,
+                st, ev))
+            return self.streams[2]
         _check("moe_layer_fwd_host", load_library().moe_layer_fwd_host(
             ctypes.byref(self.shape), n, xs, ys, aux, _ptr(gate, torch.bfloat16, "gate"),
             _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
@@ -368,6 +391,14 @@ def moe_layer_fwd_host(pipeline: HostPipeline, x_host, y_host, gate, gate_bias, 
                        aux_host=None, dev_status=None):
     """C-ABI name for HostPipeline.run."""
     return pipeline.run(x_host, y_host, gate, gate_bias, W1, W2, aux_host, dev_status)
+
+
+def moe_layer_fwd_host_fp8(pipeline: HostPipeline, x_host, y_host, gate, gate_bias,
+                           q: "Fp8Weights", aux_host=None, dev_status=None):
+    """C-ABI name for HostPipeline(fp8=True).run with quantised weights."""
+    if not pipeline.fp8:
+        raise ValueError("the pipeline was not made with fp8=True")
+    return pipeline.run(x_host, y_host, gate, gate_bias, q, None, aux_host, dev_status)
 
 
 def moe_route_gumbel(shape, x, gate, gate_bias, noise_u, temperature, topk_idx, topk_w,

@@ -949,34 +949,52 @@ moe_status moe_layer_fwd_fp8(const moe_shape* s, const moe_bf16* x, const moe_bf
                    stream, events, Noise{nullptr, 1.0f}, &q);
 }
 
+static size_t host_ws_bytes(const Dims& d, bool fp8) {
+  const size_t io = (static_cast<size_t>(d.T) * d.H * 2 + 255) & ~size_t(255);
+  return layout(d, nullptr, nullptr, fp8) + 4 * io + 512;
+}
+
 moe_status moe_host_workspace_size(const moe_shape* s, size_t* bytes) {
   if (bytes == nullptr) return MOE_ERR_NULL;
   MOE_TRY(check_shape(s));
-  const Dims d = dims_of(s);
-  const size_t io = (static_cast<size_t>(d.T) * d.H * 2 + 255) & ~size_t(255);
-  *bytes = layout(d, nullptr, nullptr) + 4 * io + 512;
+  *bytes = host_ws_bytes(dims_of(s), false);
   return MOE_OK;
 }
 
-moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
-                              moe_bf16* const* y_host, float* aux_host, const moe_bf16* gate,
-                              const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
-                              uint32_t* dev_status, void* ws, size_t ws_bytes,
-                              void* const* streams, void* const* events) {
+moe_status moe_host_workspace_size_fp8(const moe_shape* s, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_NULL;
+  MOE_TRY(check_shape(s));
+  *bytes = host_ws_bytes(dims_of(s), true);
+  return MOE_OK;
+}
+
+// The three-stream micro-batch pipeline around one device layer call (bf16
+// weights, or FP8 weights when q is set).
+static moe_status layer_fwd_host(const moe_shape* s, int64_t n_micro,
+                                 const moe_bf16* const* x_host, moe_bf16* const* y_host,
+                                 float* aux_host, const moe_bf16* gate, const float* gate_bias,
+                                 const moe_bf16* W1, const moe_bf16* W2, const Fp8Weights* q,
+                                 uint32_t* dev_status, void* ws, size_t ws_bytes,
+                                 void* const* streams, void* const* events) {
   MOE_TRY(check_shape(s));
   if (n_micro < 0) return MOE_ERR_SHAPE;
   if (x_host == nullptr || y_host == nullptr || streams == nullptr || events == nullptr)
     return MOE_ERR_NULL;
   MOE_REQUIRE(gate);
-  MOE_REQUIRE(W1);
-  MOE_REQUIRE(W2);
+  if (q == nullptr) {
+    MOE_REQUIRE(W1);
+    MOE_REQUIRE(W2);
+  } else {
+    MOE_REQUIRE(q->W1q);
+    MOE_REQUIRE(q->w1s);
+    MOE_REQUIRE(q->W2q);
+    MOE_REQUIRE(q->w2s);
+  }
   MOE_OPTIONAL(gate_bias);
   MOE_OPTIONAL(dev_status);
   if (ws == nullptr) return MOE_ERR_NULL;
   if (!aligned16(ws)) return MOE_ERR_ALIGN;
-  size_t need = 0;
-  MOE_TRY(moe_host_workspace_size(s, &need));
-  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < host_ws_bytes(dims_of(s), q != nullptr)) return MOE_ERR_WORKSPACE;
   for (int i = 0; i < 3; ++i)
     if (streams[i] == nullptr) return MOE_ERR_NULL;
   for (int i = 0; i < 6; ++i)
@@ -985,7 +1003,7 @@ moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf1
     if (x_host[i] == nullptr || y_host[i] == nullptr) return MOE_ERR_NULL;
 
   const Dims d = dims_of(s);
-  const size_t layer_bytes = layout(d, nullptr, nullptr);
+  const size_t layer_bytes = layout(d, nullptr, nullptr, q != nullptr);
   const size_t tok_bytes = static_cast<size_t>(d.T) * d.H * 2;
   const size_t io = (tok_bytes + 255) & ~size_t(255);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -1013,9 +1031,9 @@ moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf1
     // the layer: needs its tokens, and output buffer b drained (i-2 copied out)
     MOE_CUDA(cudaStreamWaitEvent(sc, ev_in[b], 0));
     if (i >= 2) MOE_CUDA(cudaStreamWaitEvent(sc, ev_out[b], 0));
-    MOE_TRY(moe_layer_fwd(s, xbuf[b], gate, gate_bias, W1, W2, ybuf[b], auxbuf[b], nullptr,
-                          nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dev_status, ws,
-                          layer_bytes, sc, nullptr));
+    MOE_TRY(layer_fwd(s, xbuf[b], gate, gate_bias, W1, W2, ybuf[b], auxbuf[b], nullptr, nullptr,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, dev_status, ws, layer_bytes, sc,
+                      nullptr, Noise{nullptr, 1.0f}, q));
     MOE_CUDA(cudaEventRecord(ev_layer[b], sc));
     // outputs out
     MOE_CUDA(cudaStreamWaitEvent(sout, ev_layer[b], 0));
@@ -1026,6 +1044,26 @@ moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf1
     MOE_CUDA(cudaEventRecord(ev_out[b], sout));
   }
   return MOE_OK;
+}
+
+moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf16* const* x_host,
+                              moe_bf16* const* y_host, float* aux_host, const moe_bf16* gate,
+                              const float* gate_bias, const moe_bf16* W1, const moe_bf16* W2,
+                              uint32_t* dev_status, void* ws, size_t ws_bytes,
+                              void* const* streams, void* const* events) {
+  return layer_fwd_host(s, n_micro, x_host, y_host, aux_host, gate, gate_bias, W1, W2, nullptr,
+                        dev_status, ws, ws_bytes, streams, events);
+}
+
+moe_status moe_layer_fwd_host_fp8(const moe_shape* s, int64_t n_micro,
+                                  const moe_bf16* const* x_host, moe_bf16* const* y_host,
+                                  float* aux_host, const moe_bf16* gate, const float* gate_bias,
+                                  const uint8_t* W1q, const float* w1_scale, const uint8_t* W2q,
+                                  const float* w2_scale, uint32_t* dev_status, void* ws,
+                                  size_t ws_bytes, void* const* streams, void* const* events) {
+  const Fp8Weights q{W1q, w1_scale, W2q, w2_scale};
+  return layer_fwd_host(s, n_micro, x_host, y_host, aux_host, gate, gate_bias, nullptr, nullptr,
+                        &q, dev_status, ws, ws_bytes, streams, events);
 }
 
 }  // extern "C"
