@@ -340,6 +340,18 @@ def test_layer_fp8_full_size_sampled():
                      check_experts=[0, w.E - 1])
 
 
+@pytest.mark.parametrize("name,n", [("fine_grained", 256), ("many_expert", 96)])
+def test_layer_fp8_full_size_sampled_other_workloads(name, n):
+    """The fine-grained and many-expert workloads at full size through the FP8
+    layer: routing and permutation in full, outputs on sampled tokens (the
+    oracle quantises only the experts those tokens reach)."""
+    w = W.get(name)
+    inp = W.make_inputs(w, seed=0)
+    g, Q = _layer_fp8_gpu(w, inp)
+    _check_layer_fp8(w, inp, g, Q, sample=W.sample_rows(w.T, n, seed=2).numpy(),
+                     check_experts=[0, w.E // 2, w.E - 1])
+
+
 def test_fp8_nan_rows_past_the_kept_rows_do_not_leak():
     """Rows of the dispatch buffer past offsets[E] are never read into a
     kept row's output (checked with NaN bytes there)."""

@@ -651,3 +651,42 @@ def test_layer_gumbel_against_oracle():
     ref = O.token_outputs(np64(inp["x"][torch.from_numpy(rows)]), r.idx[rows], r.w[rows], kept,
                           _Lazy64(inp["W1"]), _Lazy64(inp["W2"]))
     assert_ffn_close(np64(y.cpu()[torch.from_numpy(rows)]), ref, "gumbel layer y")
+
+
+def test_layer_gumbel_full_size_sampled():
+    """The many-expert workload at full size with the training router (the
+    scores written back to TMEM once): routing and the permutation in full,
+    outputs on 512 sampled tokens."""
+    w = W.get("many_expert")
+    inp = W.make_inputs(w, seed=0)
+    u = _uniforms(w.T, w.E, seed=5)
+    tau = 1.0
+    s = _shape(w.T, w.H, w.E, w.k, w.h, w.cf)
+    ws = moe.Workspace(s)
+    y = _zeros((w.T, w.H), torch.bfloat16)
+    idx = _zeros((w.T, w.k), torch.int32)
+    dest = _zeros((w.T, w.k), torch.int32)
+    st = _status()
+    dv = {n: v.to(DEV) for n, v in inp.items() if v is not None}
+    moe.moe_layer_fwd_gumbel(s, dv["x"], dv["gate"], dv["bias"], u.to(DEV), tau, dv["W1"], dv["W2"],
+                             y, topk_idx=idx, dest_row=dest, dev_status=st, ws=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lg = oracle_logits_chunked(inp["x"], inp["gate"], inp["bias"])
+    r = O.route_gumbel(lg, u.numpy(), tau, w.k)
+    d = O.dispatch_plan(r.idx, w.E, O.capacity(w.T, w.E, w.k, w.cf))
+    gidx = idx.cpu().numpy()
+    z = (lg.astype(np.float64) + O.gumbel_noise(u.numpy())) / tau
+    mism = np.nonzero((gidx != r.idx).any(axis=1))[0]
+    assert (topk_margins(z, w.k)[mism] < NEAR_TIE * (1 + np.abs(z).max())).all()
+    if len(mism) == 0:
+        assert np.array_equal(dest.cpu().numpy(), d.dest_row)
+    rows = W.sample_rows(w.T, 512, seed=3).numpy()
+    same = (gidx[rows] == r.idx[rows]).all(1) & \
+        ((dest.cpu().numpy()[rows] >= 0) == (d.dest_row[rows] >= 0)).all(1)
+    assert same.mean() > 0.99
+    rows = rows[same]
+    kept = d.dest_row[rows] >= 0
+    ref = O.token_outputs(np64(inp["x"][torch.from_numpy(rows)]), r.idx[rows], r.w[rows], kept,
+                          _Lazy64(inp["W1"]), _Lazy64(inp["W2"]))
+    assert_ffn_close(np64(y.cpu()[torch.from_numpy(rows)]), ref, "gumbel many_expert y")

@@ -79,30 +79,45 @@ __global__ void weight_amax_kernel(const uint16_t* __restrict__ W, uint32_t* __r
   atomicMax(&amax[static_cast<size_t>(e) * N + n], __float_as_uint(m));
 }
 
-// Pass 2: quantise and transpose through a 32 x 32 shared tile:
-// Wq [E, N, K] (each output column a row, contiguous over K).
-__global__ void weight_quant_kernel(const uint16_t* __restrict__ W, const uint32_t* __restrict__ amax,
-                                    uint8_t* __restrict__ Wq, int K, int N) {
-  __shared__ float tile[32][33];
+// Pass 2: quantise and transpose through a 64 x 64 shared tile: Wq [E, N, K]
+// (each output column a row, contiguous over K). Reads are 128-byte rows of
+// W; each thread then converts 16 consecutive k of one column and writes
+// them as one 16-byte vector.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __restrict__ W,
+                                                           const uint32_t* __restrict__ amax,
+                                                           uint8_t* __restrict__ Wq, int K,
+                                                           int N) {
+  __shared__ float tile[64][65];
   const int e = blockIdx.z;
-  const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int r = ty; r < 32; r += 8) {
-    const int k = k0 + r, n = n0 + tx;
-    float v = 0.f;
-    if (k < K && n < N) v = __uint_as_float(static_cast<uint32_t>(W[(static_cast<size_t>(e) * K + k) * N + n]) << 16);
-    tile[r][tx] = v;
-  }
-  __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int n = n0 + r, k = k0 + tx;
-    if (n < N && k < K) {
-      const float am = __uint_as_float(amax[static_cast<size_t>(e) * N + n]);
-      const float inv = am > 0.f ? kE4M3Max / am : 0.f;
-      const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(tile[tx][r] * inv, __NV_SATFINITE, __NV_E4M3);
-      Wq[(static_cast<size_t>(e) * N + n) * K + k] = static_cast<uint8_t>(q);
+  const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  const int tid = threadIdx.x;
+  // load: 64 rows (k) x 64 columns (n); thread = (row tid / 4, 16 columns as
+  // two 16-byte vectors). K and N are multiples of 64 (checked by the host).
+  {
+    const int r = tid >> 2, cq = (tid & 3) * 16;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        W + (static_cast<size_t>(e) * K + k0 + r) * N + n0 + cq);
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      tile[r][cq + 2 * i] = bf16_lo(w[i]);
+      tile[r][cq + 2 * i + 1] = bf16_hi(w[i]);
     }
   }
+  __syncthreads();
+  // store: column n = tid / 4, k range (tid % 4) * 16 .. +16
+  const int c = tid >> 2, kq = (tid & 3) * 16;
+  const int n = n0 + c;
+  const float am = __uint_as_float(amax[static_cast<size_t>(e) * N + n]);
+  const float inv = am > 0.f ? kE4M3Max / am : 0.f;
+  uint32_t w4[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w4[j] = fp8x4(tile[kq + 4 * j][c] * inv, tile[kq + 4 * j + 1][c] * inv,
+                  tile[kq + 4 * j + 2][c] * inv, tile[kq + 4 * j + 3][c] * inv);
+  *reinterpret_cast<uint4*>(Wq + (static_cast<size_t>(e) * N + n) * K + k0 + kq) =
+      make_uint4(w4[0], w4[1], w4[2], w4[3]);
 }
 
 // Pass 3: the maxima become the dequantisation scales, in place.
@@ -320,8 +335,8 @@ cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, i
   dim3 g1((N + 255) / 256, (K + k_chunk - 1) / k_chunk, E);
   weight_amax_kernel<<<g1, 256, 0, st>>>(W, amax, K, N, k_chunk);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  dim3 g2((N + 31) / 32, (K + 31) / 32, E);
-  weight_quant_kernel<<<g2, dim3(32, 8), 0, st>>>(W, amax, Wq, K, N);
+  dim3 g2((N + 63) / 64, (K + 63) / 64, E);
+  weight_quant_kernel<<<g2, 256, 0, st>>>(W, amax, Wq, K, N);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const int n = E * N;
   weight_scale_kernel<<<(n + 255) / 256, 256, 0, st>>>(Ws, n);
