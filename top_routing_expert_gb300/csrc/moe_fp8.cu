@@ -318,7 +318,7 @@ cudaError_t launch_combine_fp8(const CombineArgs& a, const uint8_t* y_q, const f
   int grid = (a.T + 7) / 8;
   if (grid > num_sms * 8) grid = num_sms * 8;
   if (a.k <= 2)
-    combine_fp8_kernel<2, 2><<<grid, 256, 0, st>>>(a, y_q, y_scale);
+    combine_fp8_kernel<2, 3><<<grid, 256, 0, st>>>(a, y_q, y_scale);
   else if (a.k <= 4)
     combine_fp8_kernel<4, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
   else
