@@ -459,7 +459,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=W.WORKLOAD_ORDER + list(W.PROFILE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=4096)
+    ap.add_argument("--cpu-tokens", type=int, default=6144)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fp8", action="store_true",
