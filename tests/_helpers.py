@@ -7,7 +7,7 @@ import torch
 
 from oracle import moe_oracle as O
 
-# spec floating-point bars for bf16-in / fp32-accumulate outputs
+# floating-point bars for bf16-in / fp32-accumulate outputs
 FFN_MAX_REL = 2e-2      # max|err| <= 2e-2 * max|ref|
 FFN_MEAN_REL = 5e-3     # sum|err| <= 5e-3 * sum|ref|   (mean relative error)
 W_ABS = 1e-6            # routing weights
