@@ -296,6 +296,13 @@ def test_layer_fp8_edge_shapes(T, H, E, k, h, cf, bias):
     _check_layer_fp8(w, inp, g, Q)
 
 
+def test_layer_fp8_maximum_experts_and_k():
+    w = W.custom(1024, 128, 256, 8, 128, 1.5, "normal1.5", name="fp8maxE")
+    inp = W.make_inputs(w, seed=7)
+    g, Q = _layer_fp8_gpu(w, inp)
+    _check_layer_fp8(w, inp, g, Q, check_experts=[0, 255])
+
+
 def test_layer_fp8_deterministic_and_chain():
     """Two layer calls give the same bits, and permute_fp8 -> expert_ffn_fp8
     (e4m3 outputs) -> combine_fp8 through the separate entry points gives

@@ -118,6 +118,45 @@ def test_route_logits_full_size_workloads(name):
 
 # ============================================================ router GEMM ==
 
+@pytest.mark.parametrize("E,k", [(12, 3), (64, 6), (256, 8)])
+def test_router_persistent_against_oracle(E, k):
+    """More 128-token tiles than SMs (the persistent router: stage ring across
+    tiles, two TMEM accumulators), including the largest E and k."""
+    T, H = 160 * 128 + 77, 256
+    gen = torch.Generator().manual_seed(E + k)
+    x = torch.randn((T, H), generator=gen).to(torch.bfloat16)
+    gate = (torch.randn((H, E), generator=gen) / H ** 0.5).to(torch.bfloat16)
+    bias = torch.randn(E, generator=gen) * 0.5
+    s = _shape(T, H, E, k, 64, 1.0)
+    ws = moe.Workspace(s)
+    idx = _zeros((T, k), torch.int32)
+    wt = _zeros((T, k), torch.float32)
+    routed = _zeros(E, torch.int32)
+    P = _zeros(E, torch.float32)
+    aux = _zeros(1, torch.float32)
+    lg = _zeros((T, E), torch.float32)
+    st = _status()
+    moe.moe_route(s, x.to(DEV), gate.to(DEV), bias.to(DEV), idx, wt, routed, P, aux, lg, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_lg = O.router_logits(np64(x), np64(gate), bias.numpy())
+    got_lg = lg.cpu().numpy().astype(np.float64)
+    assert np.abs(got_lg - ref_lg).max() <= 1e-4 * (1 + np.abs(ref_lg).max())
+    # routing against the oracle's own logits: differences only on near-ties
+    r = O.route_from_logits(ref_lg.astype(np.float32), k)
+    gidx = idx.cpu().numpy()
+    mism = (gidx != r.idx).any(axis=1)
+    assert (topk_margins(ref_lg, k)[mism] < NEAR_TIE).all()
+    # weights: fp32 logits within 1e-4 relative of float64 ones move w by
+    # at most a few 1e-5
+    assert np.abs(wt.cpu().numpy()[~mism] - r.w[~mism]).max() <= 1e-4
+    st_ref = O.load_balance_stats(r.idx, r.p, E)
+    if not mism.any():
+        assert np.array_equal(routed.cpu().numpy(), st_ref.routed)
+    assert np.allclose(P.cpu().numpy(), st_ref.P, rtol=1e-3, atol=1e-6)
+    assert abs(float(aux.item()) - st_ref.aux) <= 1e-3 * st_ref.aux
+
+
 def _route_gpu(s, x, gate, bias):
     T, E, k = s.T, s.E, s.top_k
     ws = moe.Workspace(s)
@@ -480,6 +519,15 @@ def test_layer_named_small_workloads(name):
 def test_layer_edge_shapes(T, H, E, k, h, cf, bias):
     w = W.custom(T, H, E, k, h, cf, bias, name=f"edge{T}_{E}_{k}")
     inp = W.make_inputs(w, seed=T)
+    g = _layer_gpu(w, inp)
+    _check_layer(w, inp, g)
+
+
+def test_layer_maximum_experts_and_k():
+    """E = 256, k = 8 (the supported maximum) with 8192 assignments: the
+    CTA-pair GEMM with the 6-stage ring (7 stages need E <= 234)."""
+    w = W.custom(1024, 128, 256, 8, 128, 1.5, "normal1.5", name="maxE")
+    inp = W.make_inputs(w, seed=7)
     g = _layer_gpu(w, inp)
     _check_layer(w, inp, g)
 
