@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 // slot's vectors are loaded before any is used, so a token's k row reads are
 // in flight together.
 template <int KMAX, int U>
-__global__ void __launch_bounds__(256, 3) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(256, (KMAX * U > 8) ? 2 : 3) combine_kernel(CombineArgs a) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 3;
@@ -282,6 +282,8 @@ cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
     combine_kernel<2, 4><<<grid, 256, 0, st>>>(a);
   else if (a.k <= 4)
     combine_kernel<4, 2><<<grid, 256, 0, st>>>(a);
+  else if (a.k <= 6)
+    combine_kernel<6, 2><<<grid, 256, 0, st>>>(a);
   else
     combine_kernel<8, 1><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();

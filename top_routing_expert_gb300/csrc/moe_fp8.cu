@@ -321,6 +321,8 @@ cudaError_t launch_combine_fp8(const CombineArgs& a, const uint8_t* y_q, const f
     combine_fp8_kernel<2, 3><<<grid, 256, 0, st>>>(a, y_q, y_scale);
   else if (a.k <= 4)
     combine_fp8_kernel<4, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
+  else if (a.k <= 6)
+    combine_fp8_kernel<6, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
   else
     combine_fp8_kernel<8, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
   return cudaGetLastError();
