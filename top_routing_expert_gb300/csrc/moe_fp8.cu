@@ -197,15 +197,39 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(GatherArgs a, uint8_t* 
     }
     if (!any) continue;
     const uint4* src = reinterpret_cast<const uint4*>(a.x) + static_cast<size_t>(t) * nvec;
+    // both passes keep kGatherU 16-byte loads per lane in flight (the second
+    // pass re-reads the row from cache)
+    constexpr int kGatherU = 4;
     float m = 0.f;
-    for (int i = lane; i < nvec; i += 32) m = fmaxf(m, amax8(__ldg(src + i)));
+    for (int b = 0; b < nvec; b += 32 * kGatherU) {
+      uint4 v[kGatherU];
+#pragma unroll
+      for (int u = 0; u < kGatherU; ++u) {
+        const int i = b + 32 * u + lane;
+        v[u] = i < nvec ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherU; ++u) m = fmaxf(m, amax8(v[u]));
+    }
     m = warp_max(m);
     const float inv = m > 0.f ? kE4M3Max / m : 0.f;
-    for (int i = lane; i < nvec; i += 32) {
-      const uint2 q = quant8(__ldg(src + i), inv);
+    for (int b = 0; b < nvec; b += 32 * kGatherU) {
+      uint4 v[kGatherU];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (d[j] >= 0) reinterpret_cast<uint2*>(xq + static_cast<size_t>(d[j]) * a.H)[i] = q;
+      for (int u = 0; u < kGatherU; ++u) {
+        const int i = b + 32 * u + lane;
+        if (i < nvec) v[u] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherU; ++u) {
+        const int i = b + 32 * u + lane;
+        if (i < nvec) {
+          const uint2 q = quant8(v[u], inv);
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (d[j] >= 0) reinterpret_cast<uint2*>(xq + static_cast<size_t>(d[j]) * a.H)[i] = q;
+        }
+      }
     }
     if (lane < a.k && dest >= 0) xs[dest] = m / kE4M3Max;
   }
