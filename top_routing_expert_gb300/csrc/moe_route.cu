@@ -405,8 +405,10 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
   return s;
 }
 
-// Up to 512 threads two CTAs share an SM (one's epilogue overlaps the
-// other's loads); the register budget allows that at 64 per thread.
+// One CTA per 128-token tile; the launcher picks this kernel when there are
+// no more tiles than SMs (the persistent kernel takes larger batches).
+// Stages are sized so that two CTAs could share an SM; with one CTA per SM,
+// up to 8 stages measured the same on the fine-grained router (46 us).
 template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens * 8, 1)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -810,7 +812,7 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 // ------------------------------------------------------------------ host ----
 
 int route_stages(int E_pad) {
-  // as many stages as fit in ~108 KB, so that two CTAs share an SM
+  // as many stages as fit in ~108 KB (two CTAs' worth per SM)
   const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
   int s = (108 * 1024) / stage;
   return s < 2 ? 2 : (s > 6 ? 6 : s);
