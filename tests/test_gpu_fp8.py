@@ -445,3 +445,38 @@ def test_layer_fp8_host_pipeline_equals_device_layer():
         torch.cuda.synchronize()
         assert torch.equal(y.cpu(), y_host[i]), i
         assert float(aux.item()) == float(aux_host[i])
+
+
+def test_layer_fp8_captured_in_a_cuda_graph():
+    """The FP8 layer (its memset node included) replays from a CUDA graph with
+    the direct call's bits."""
+    w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="graph8")
+    s = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
+    base = W.make_inputs(w, seed=51)
+    gate, bias = base["gate"].to(DEV), base["bias"].to(DEV)
+    Q = moe.Fp8Weights(base["W1"].to(DEV), base["W2"].to(DEV))
+    ws = moe.Workspace(s, fp8=True)
+    x_static = base["x"].to(DEV)
+    y_static = _zeros((w.T, w.H), torch.bfloat16)
+
+    def layer():
+        moe.moe_layer_fwd_fp8(s, x_static, gate, bias, Q, y_static, ws=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            layer()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer()
+    ws_direct = moe.Workspace(s, fp8=True)
+    for seed in (52, 53):
+        x = W.make_inputs(w, seed=seed, with_weights=False)["x"].to(DEV)
+        x_static.copy_(x)
+        g.replay()
+        y = _zeros((w.T, w.H), torch.bfloat16)
+        moe.moe_layer_fwd_fp8(s, x, gate, bias, Q, y, ws=ws_direct)
+        torch.cuda.synchronize()
+        assert torch.equal(y_static, y), seed

@@ -738,3 +738,43 @@ def test_layer_gumbel_full_size_sampled():
     ref = O.token_outputs(np64(inp["x"][torch.from_numpy(rows)]), r.idx[rows], r.w[rows], kept,
                           _Lazy64(inp["W1"]), _Lazy64(inp["W2"]))
     assert_ffn_close(np64(y.cpu()[torch.from_numpy(rows)]), ref, "gumbel many_expert y")
+
+
+def test_layer_captured_in_a_cuda_graph():
+    """moe_layer_fwd enqueues only asynchronous work (no allocation, no host
+    synchronisation), so it can be captured in a CUDA graph: replays with
+    new tokens copied into the captured input give the direct calls' bits."""
+    w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="graph")
+    s = _shape(w.T, w.H, w.E, w.k, w.h, w.cf)
+    base = W.make_inputs(w, seed=41)
+    dv = {n: base[n].to(DEV) for n in ("gate", "W1", "W2", "bias")}
+    ws = moe.Workspace(s)
+    x_static = base["x"].to(DEV)
+    y_static = _zeros((w.T, w.H), torch.bfloat16)
+    aux_static = _zeros(1, torch.float32)
+
+    def layer():
+        moe.moe_layer_fwd(s, x_static, dv["gate"], dv["bias"], dv["W1"], dv["W2"], y_static,
+                          aux=aux_static, ws=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            layer()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer()
+    ws_direct = moe.Workspace(s)
+    for seed in (42, 43, 44):
+        x = W.make_inputs(w, seed=seed, with_weights=False)["x"].to(DEV)
+        x_static.copy_(x)
+        g.replay()
+        y = _zeros((w.T, w.H), torch.bfloat16)
+        aux = _zeros(1, torch.float32)
+        moe.moe_layer_fwd(s, x, dv["gate"], dv["bias"], dv["W1"], dv["W2"], y, aux=aux,
+                          ws=ws_direct)
+        torch.cuda.synchronize()
+        assert torch.equal(y_static, y), seed
+        assert torch.equal(aux_static, aux), seed
