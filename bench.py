@@ -154,25 +154,25 @@ def run_ours(args, rank, world, local_rank):
         q = moe.Fp8Weights(d["W1"], d["W2"])
         torch.cuda.synchronize(dev)
 
-        def step(events=None):
+        def step(events=None, strm=None):
             moe.moe_layer_fwd_fp8(s, d["x"], d["gate"], d["bias"], q, y, aux=aux,
                                   offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
-                                  stream=stream, events=events)
+                                  stream=strm or stream, events=events)
     elif args.gumbel is None:
-        def step(events=None):
+        def step(events=None, strm=None):
             moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y, aux=aux,
                               offsets=offsets, dest_row=dest, dev_status=status, ws=ws,
-                              stream=stream, events=events)
+                              stream=strm or stream, events=events)
     else:
         # the training router: uniforms drawn once, outside the timed region
         gen = torch.Generator(device=dev).manual_seed(rank + 1)
         noise = torch.rand((T, E), generator=gen, device=dev, dtype=torch.float32)
 
-        def step(events=None):
+        def step(events=None, strm=None):
             moe.moe_layer_fwd_gumbel(s, d["x"], d["gate"], d["bias"], noise, args.gumbel,
                                      d["W1"], d["W2"], y, aux=aux, offsets=offsets,
-                                     dest_row=dest, dev_status=status, ws=ws, stream=stream,
-                                     events=events)
+                                     dest_row=dest, dev_status=status, ws=ws,
+                                     stream=strm or stream, events=events)
 
     for _ in range(args.warmup):
         step()
@@ -225,12 +225,53 @@ def run_ours(args, rank, world, local_rank):
         run_e2e(args, moe, s, inp, d, y, aux, ws, stream, dev, world, q)
     dense = None if (args.fp8 or args.gumbel is not None) else \
         run_dense_ffn(args, moe, w, d, stream, dev, flush is not None)
+    graph = run_graph(args, step, stream, dev, flush) if args.graph else None
     if rank != 0:
         return None
     l2 = (f"L2 flushed between steps ({2 * L2_BYTES >> 20} MB write); steps timed by their own events"
           if flush is not None else
           f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB re-read per step); no flush")
-    return report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2, dense)
+    line = report(args, w, world, ms, stage_ms, clk, st, n_kept, any_kept, e2e, inp, l2, dense)
+    if graph is not None:
+        line["graph_replay"] = {"ms_per_step": round(graph, 4),
+                                "value": round(w.T * world / (graph / 1e3), 1), "unit": "tokens/s",
+                                "what": "the same step captured once in a CUDA graph and replayed"}
+    return line
+
+
+def run_graph(args, step, stream, dev, flush):
+    """The same layer step captured once in a CUDA graph and replayed: the
+    host's launch work leaves the loop (it matters for the small,
+    launch-bound layers). Timed like the main loop, without per-stage
+    events."""
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(strm=side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(strm=torch.cuda.current_stream(dev))
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    cur = torch.cuda.current_stream(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(float(i))
+        ev[i][0].record(cur)
+        g.replay()
+        ev[i][1].record(cur)
+    t1.record(cur)
+    torch.cuda.synchronize(dev)
+    if flush is None:
+        return t0.elapsed_time(t1) / args.steps
+    return sum(a.elapsed_time(b) for a, b in ev) / args.steps
 
 
 def run_dense_ffn(args, moe, w, d, stream, dev, flush_l2):
@@ -466,6 +507,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=6144)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 (e4m3) dispatch and expert FFN (weights quantised before timing)")
     ap.add_argument("--gumbel", type=float, default=None, metavar="TAU",
