@@ -74,3 +74,24 @@ def test_gpu_arm_report_has_the_contract_keys():
     assert line["clocks"]["reasons"] == ["sw_power_cap"]
     assert line["moe_vs_dense_ffn"]["ratio"] == round(sum(stage) / 4.6, 3)
     json.dumps(line)  # serialisable
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched with torchrun for N = 2 on 127.0.0.1: rank 0 alone runs the
+    oracle and prints the line; the other rank exits 0."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "1", "--cpu-tokens", "32"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.strip().splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    _check_base(line)
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
