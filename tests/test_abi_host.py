@@ -218,3 +218,23 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
     assert lib.moe_combine_fp8(ctypes.byref(s), f, P(FAKE + 4), f, f, f, None) == 5
     assert lib.moe_permute_fp8(ctypes.byref(s), f, f, None, f, f, None, f, None, None, f, n,
                                None) == 1
+
+
+def test_binding_sizes_every_tensor_argument():
+    """Every tensor the binding hands to a shaped entry point has a minimum
+    element count derived from the shape (the C ABI takes bare pointers and
+    cannot check sizes), and the counts follow the header's layouts."""
+    import inspect
+    src = inspect.getsource(moe)
+    names = set(re.findall(r'_arg\([a-z_.]+, [A-Za-z0-9_.]+, torch\.[a-z0-9]+, "([A-Za-z0-9_]+)"\)',
+                           src))
+    assert len(names) >= 30
+    s = moe.MoeShape.make(1000, 384, 12, 3, 320, 1.0)
+    A = 1000 * 3
+    want = {"x": 1000 * 384, "gate": 384 * 12, "offsets": 13, "dest_row": A, "x_perm": A * 384,
+            "act": A * 320, "W1": 12 * 384 * 320, "W2q": 12 * 384 * 320, "w1_scale": 12 * 320,
+            "y_scale": A * 3, "noise_u": 1000 * 12, "aux": 1}
+    for n in names:
+        assert moe._need(s, n) >= 1, n
+    for n, v in want.items():
+        assert moe._need(s, n) == v, n

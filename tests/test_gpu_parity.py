@@ -547,6 +547,32 @@ def test_layer_empty_batch():
     del w
 
 
+def test_binding_refuses_undersized_or_mistyped_buffers():
+    """The C ABI takes bare pointers; the binding refuses a buffer smaller
+    than the shape needs, or of the wrong dtype, before anything launches."""
+    T, H, E, k, h = 64, 64, 4, 2, 64
+    s = _shape(T, H, E, k, h, 1.0)
+    ws = moe.Workspace(s)
+    x = _zeros((T, H), torch.bfloat16)
+    gate = _zeros((H, E), torch.bfloat16)
+    W1 = _zeros((E, H, h), torch.bfloat16)
+    W2 = _zeros((E, h, H), torch.bfloat16)
+    y_short = torch.full((T * H - 1,), 7.0, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError, match="y holds"):
+        moe.moe_layer_fwd(s, x, gate, None, W1, W2, y_short, ws=ws)
+    with pytest.raises(ValueError, match="W2 holds"):
+        moe.moe_layer_fwd(s, x, gate, None, W1, W2[:, :h - 1].contiguous(),
+                          _zeros((T, H), torch.bfloat16), ws=ws)
+    with pytest.raises(ValueError, match="must be torch.bfloat16"):
+        moe.moe_layer_fwd(s, x.float(), gate, None, W1, W2, _zeros((T, H), torch.bfloat16),
+                          ws=ws)
+    with pytest.raises(ValueError, match="offsets holds"):
+        moe.moe_layer_fwd(s, x, gate, None, W1, W2, _zeros((T, H), torch.bfloat16),
+                          offsets=_zeros(E, torch.int32), ws=ws)
+    torch.cuda.synchronize()
+    assert (y_short.float().cpu() == 7.0).all()
+
+
 def test_layer_is_deterministic_and_reuses_workspace():
     w = W.get("imbalanced")
     inp = W.make_inputs(w, seed=1)

@@ -57,10 +57,12 @@ def test_noalloc_permute_matches_workspace_permute_twice_in_a_row():
 
 
 def test_noalloc_rejects_shapes_beyond_its_static_scratch():
-    s = moe.MoeShape.make(131072, 64, 128, 2, 64, 1.1)   # needs > 1 MiB of scratch
-    one_i = torch.zeros((1, 2), dtype=torch.int32, device=DEV)
-    one_x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
-    offs = torch.zeros(129, dtype=torch.int32, device=DEV)
+    T, H, E, k = 131072, 64, 128, 2
+    s = moe.MoeShape.make(T, H, E, k, 64, 1.1)   # needs > 1 MiB of scratch
+    idx = torch.zeros((T, k), dtype=torch.int32, device=DEV)
+    x = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    xp = torch.zeros((T * k, H), dtype=torch.bfloat16, device=DEV)
+    offs = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
     with pytest.raises(moe.MoeError) as e:
-        moe.moe_permute_noalloc(s, one_x, one_i, None, offs, one_i, None, one_x)
+        moe.moe_permute_noalloc(s, x, idx, None, offs, torch.empty_like(idx), None, xp)
     assert e.value.code == 3

@@ -123,16 +123,47 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
 
 # ------------------------------------------------------------ helpers ----
 
-def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor", numel: Optional[int] = None
+         ) -> Optional[int]:
+    """Device address of a contiguous CUDA tensor of `dtype` on the current
+    device holding at least `numel` elements (the C ABI takes bare pointers
+    and cannot check sizes, so an undersized buffer is refused here)."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the shape needs {numel}")
     return t.data_ptr()
+
+
+def _need(s: "MoeShape", name: str) -> int:
+    """Elements the named argument must hold for shape s (layouts as in
+    include/moe_gb300.h)."""
+    T, H, E, k, h = s.T, s.H, s.E, s.top_k, s.h
+    A = T * k
+    return {
+        "x": T * H, "y": T * H, "gate": H * E, "gate_bias": E, "noise_u": T * E,
+        "logits": T * E, "logits_out": T * E, "scores_out": T * E,
+        "topk_idx": A, "topk_w": A, "dest_row": A, "src_token": A,
+        "routed_counts": E, "P": E, "kept_counts": E, "offsets": E + 1,
+        "aux": 1, "dev_status": 1,
+        "x_perm": A * H, "y_perm": A * H, "act": A * h, "x_q": A * H, "y_q": A * H,
+        "x_scale": A, "y_scale": A * ((H + 127) // 128),
+        "W1": E * H * h, "W2": E * h * H, "W1q": E * h * H, "W2q": E * H * h,
+        "w1_scale": E * h, "w2_scale": E * H,
+    }[name]
+
+
+def _arg(s: "MoeShape", t: Optional[torch.Tensor], dtype, name: str) -> Optional[int]:
+    return _ptr(t, dtype, name, None if t is None else _need(s, name))
 
 
 def _stream(stream) -> Optional[int]:
@@ -217,11 +248,13 @@ def moe_route(shape, x, gate, gate_bias, topk_idx, topk_w, routed_counts=None, P
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_route", load_library().moe_route(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
-        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
-        _ptr(P, torch.float32, "P"), _ptr(aux, torch.float32, "aux"),
-        _ptr(logits_out, torch.float32, "logits_out"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
+        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"),
+        _arg(s, P, torch.float32, "P"), _arg(s, aux, torch.float32, "aux"),
+        _arg(s, logits_out, torch.float32, "logits_out"),
+        _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -230,10 +263,10 @@ def moe_route_logits(shape, logits, topk_idx, topk_w, routed_counts=None, P=None
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_route_logits", load_library().moe_route_logits(
-        ctypes.byref(s), _ptr(logits, torch.float32, "logits"),
-        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
-        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
-        _ptr(aux, torch.float32, "aux"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, logits, torch.float32, "logits"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
+        _arg(s, aux, torch.float32, "aux"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -242,10 +275,11 @@ def moe_permute(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_permute", load_library().moe_permute(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
-        _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
+        _arg(s, x_perm, torch.bfloat16, "x_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -254,10 +288,11 @@ def moe_expert_ffn(shape, x_perm, offsets, W1, W2, act, y_perm, dev_status=None,
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn", load_library().moe_expert_ffn(
-        ctypes.byref(s), _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(W1, torch.bfloat16, "W1"), _ptr(W2, torch.bfloat16, "W2"),
-        _ptr(act, torch.bfloat16, "act"), _ptr(y_perm, torch.bfloat16, "y_perm"),
-        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+        ctypes.byref(s), _arg(s, x_perm, torch.bfloat16, "x_perm"),
+        _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, W1, torch.bfloat16, "W1"), _arg(s, W2, torch.bfloat16, "W2"),
+        _arg(s, act, torch.bfloat16, "act"), _arg(s, y_perm, torch.bfloat16, "y_perm"),
+        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
 
 
 def moe_expert_ffn_gathered(shape, x, src_token, offsets, W1, W2, act, y_perm, dev_status=None,
@@ -267,18 +302,20 @@ def moe_expert_ffn_gathered(shape, x, src_token, offsets, W1, W2, act, y_perm, d
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn_gathered", load_library().moe_expert_ffn_gathered(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(src_token, torch.int32, "src_token"),
-        _ptr(offsets, torch.int32, "offsets"), _ptr(W1, torch.bfloat16, "W1"),
-        _ptr(W2, torch.bfloat16, "W2"), _ptr(act, torch.bfloat16, "act"),
-        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
+        _arg(s, src_token, torch.int32, "src_token"),
+        _arg(s, offsets, torch.int32, "offsets"), _arg(s, W1, torch.bfloat16, "W1"),
+        _arg(s, W2, torch.bfloat16, "W2"), _arg(s, act, torch.bfloat16, "act"),
+        _arg(s, y_perm, torch.bfloat16, "y_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_combine(shape, y_perm, dest_row, topk_w, y, stream=None):
     s = _shape(shape)
     _check("moe_combine", load_library().moe_combine(
-        ctypes.byref(s), _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(dest_row, torch.int32, "dest_row"),
-        _ptr(topk_w, torch.float32, "topk_w"), _ptr(y, torch.bfloat16, "y"), _stream(stream)))
+        ctypes.byref(s), _arg(s, y_perm, torch.bfloat16, "y_perm"),
+        _arg(s, dest_row, torch.int32, "dest_row"),
+        _arg(s, topk_w, torch.float32, "topk_w"), _arg(s, y, torch.bfloat16, "y"), _stream(stream)))
 
 
 def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None, topk_w=None,
@@ -289,13 +326,14 @@ def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None,
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd", load_library().moe_layer_fwd(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
-        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
-        _ptr(W2, torch.bfloat16, "W2"), _ptr(y, torch.bfloat16, "y"), _ptr(aux, torch.float32, "aux"),
-        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
-        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
-        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
+        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, W1, torch.bfloat16, "W1"),
+        _arg(s, W2, torch.bfloat16, "W2"), _arg(s, y, torch.bfloat16, "y"),
+        _arg(s, aux, torch.float32, "aux"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
+        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
 
 
@@ -308,10 +346,11 @@ def moe_permute_noalloc(shape, x, topk_idx, kept_counts, offsets, dest_row, src_
     make the first call on a device before any stream capture."""
     s = _shape(shape)
     _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
-        _ptr(x_perm, torch.bfloat16, "x_perm"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
+        _arg(s, x_perm, torch.bfloat16, "x_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
         _stream(stream)))
 
 
@@ -322,11 +361,13 @@ def host_workspace_size(shape) -> int:
     return n.value
 
 
-def _host_ptr(t: torch.Tensor, name: str) -> int:
+def _host_ptr(t: torch.Tensor, name: str, numel: int) -> int:
     if t.is_cuda:
         raise ValueError(f"{name} must be a host tensor")
     if not t.is_contiguous() or t.dtype != torch.bfloat16:
         raise ValueError(f"{name} must be a contiguous bf16 host tensor")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the shape needs {numel}")
     return t.data_ptr()
 
 
@@ -360,8 +401,9 @@ class HostPipeline:
         n = len(x_host)
         if len(y_host) != n:
             raise ValueError("x_host and y_host need the same length")
-        xs = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "x_host") for t in x_host])
-        ys = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "y_host") for t in y_host])
+        TH = self.shape.T * self.shape.H
+        xs = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "x_host", TH) for t in x_host])
+        ys = (ctypes.c_void_p * max(n, 1))(*[_host_ptr(t, "y_host", TH) for t in y_host])
         aux = None
         if aux_host is not None:
             if aux_host.is_cuda or aux_host.dtype != torch.float32 or aux_host.numel() < n:
@@ -372,17 +414,24 @@ class HostPipeline:
         if self.fp8:
             q = W1  # an Fp8Weights
             _check("moe_layer_fwd_host_fp8", load_library().moe_layer_fwd_host_fp8(
-                ctypes.byref(self.shape), n, xs, ys, aux, _ptr(gate, torch.bfloat16, "gate"),
-                _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(q.W1q, torch.uint8, "W1q"),
-                _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
-                _ptr(q.w2_scale, torch.float32, "w2_scale"),
-                _ptr(dev_status, torch.int32, "dev_status"), self.buf.data_ptr(), self.nbytes,
+                ctypes.byref(self.shape), n, xs, ys, aux,
+                _arg(self.shape, gate, torch.bfloat16, "gate"),
+                _arg(self.shape, gate_bias, torch.float32, "gate_bias"),
+                _arg(self.shape, q.W1q, torch.uint8, "W1q"),
+                _arg(self.shape, q.w1_scale, torch.float32, "w1_scale"),
+                _arg(self.shape, q.W2q, torch.uint8, "W2q"),
+                _arg(self.shape, q.w2_scale, torch.float32, "w2_scale"),
+                _arg(self.shape, dev_status, torch.int32, "dev_status"), self.buf.data_ptr(),
+                self.nbytes,
                 st, ev))
             return self.streams[2]
         _check("moe_layer_fwd_host", load_library().moe_layer_fwd_host(
-            ctypes.byref(self.shape), n, xs, ys, aux, _ptr(gate, torch.bfloat16, "gate"),
-            _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(W1, torch.bfloat16, "W1"),
-            _ptr(W2, torch.bfloat16, "W2"), _ptr(dev_status, torch.int32, "dev_status"),
+            ctypes.byref(self.shape), n, xs, ys, aux,
+            _arg(self.shape, gate, torch.bfloat16, "gate"),
+            _arg(self.shape, gate_bias, torch.float32, "gate_bias"),
+            _arg(self.shape, W1, torch.bfloat16, "W1"),
+            _arg(self.shape, W2, torch.bfloat16, "W2"),
+            _arg(self.shape, dev_status, torch.int32, "dev_status"),
             self.buf.data_ptr(), self.nbytes, st, ev))
         return self.streams[2]
 
@@ -408,12 +457,14 @@ def moe_route_gumbel(shape, x, gate, gate_bias, noise_u, temperature, topk_idx, 
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_route_gumbel", load_library().moe_route_gumbel(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
-        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(noise_u, torch.float32, "noise_u"),
-        float(temperature), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
-        _ptr(P, torch.float32, "P"), _ptr(aux, torch.float32, "aux"),
-        _ptr(scores_out, torch.float32, "scores_out"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
+        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, noise_u, torch.float32, "noise_u"),
+        float(temperature), _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"),
+        _arg(s, P, torch.float32, "P"), _arg(s, aux, torch.float32, "aux"),
+        _arg(s, scores_out, torch.float32, "scores_out"),
+        _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -426,14 +477,14 @@ def moe_layer_fwd_gumbel(shape, x, gate, gate_bias, noise_u, temperature, W1, W2
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd_gumbel", load_library().moe_layer_fwd_gumbel(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
-        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(noise_u, torch.float32, "noise_u"),
-        float(temperature), _ptr(W1, torch.bfloat16, "W1"), _ptr(W2, torch.bfloat16, "W2"),
-        _ptr(y, torch.bfloat16, "y"), _ptr(aux, torch.float32, "aux"),
-        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(topk_w, torch.float32, "topk_w"),
-        _ptr(routed_counts, torch.int32, "routed_counts"), _ptr(P, torch.float32, "P"),
-        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
+        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, noise_u, torch.float32, "noise_u"),
+        float(temperature), _arg(s, W1, torch.bfloat16, "W1"), _arg(s, W2, torch.bfloat16, "W2"),
+        _arg(s, y, torch.bfloat16, "y"), _arg(s, aux, torch.float32, "aux"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
+        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
 
 
@@ -445,8 +496,8 @@ def moe_quantize_weights_fp8(W, Wq, w_scale, stream=None):
         raise ValueError("W must be [E, K, N]")
     E, K, N = W.shape
     _check("moe_quantize_weights_fp8", load_library().moe_quantize_weights_fp8(
-        E, K, N, _ptr(W, torch.bfloat16, "W"), _ptr(Wq, torch.uint8, "Wq"),
-        _ptr(w_scale, torch.float32, "w_scale"), _stream(stream)))
+        E, K, N, _ptr(W, torch.bfloat16, "W"), _ptr(Wq, torch.uint8, "Wq", E * K * N),
+        _ptr(w_scale, torch.float32, "w_scale", E * N), _stream(stream)))
 
 
 class Fp8Weights:
@@ -471,11 +522,12 @@ def moe_permute_fp8(shape, x, topk_idx, kept_counts, offsets, dest_row, src_toke
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_permute_fp8", load_library().moe_permute_fp8(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(kept_counts, torch.int32, "kept_counts"), _ptr(offsets, torch.int32, "offsets"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(src_token, torch.int32, "src_token"),
-        _ptr(x_q, torch.uint8, "x_q"), _ptr(x_scale, torch.float32, "x_scale"),
-        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
+        _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
+        _arg(s, x_q, torch.uint8, "x_q"), _arg(s, x_scale, torch.float32, "x_scale"),
+        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
 
 
 def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm=None,
@@ -487,12 +539,13 @@ def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm=
     s = _shape(shape)
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn_fp8", load_library().moe_expert_ffn_fp8(
-        ctypes.byref(s), _ptr(x_q, torch.uint8, "x_q"), _ptr(x_scale, torch.float32, "x_scale"),
-        _ptr(offsets, torch.int32, "offsets"), _ptr(q.W1q, torch.uint8, "W1q"),
-        _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
-        _ptr(q.w2_scale, torch.float32, "w2_scale"), _ptr(act, torch.bfloat16, "act"),
-        _ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(y_q, torch.uint8, "y_q"),
-        _ptr(y_scale, torch.float32, "y_scale"), _ptr(dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), _arg(s, x_q, torch.uint8, "x_q"),
+        _arg(s, x_scale, torch.float32, "x_scale"),
+        _arg(s, offsets, torch.int32, "offsets"), _arg(s, q.W1q, torch.uint8, "W1q"),
+        _arg(s, q.w1_scale, torch.float32, "w1_scale"), _arg(s, q.W2q, torch.uint8, "W2q"),
+        _arg(s, q.w2_scale, torch.float32, "w2_scale"), _arg(s, act, torch.bfloat16, "act"),
+        _arg(s, y_perm, torch.bfloat16, "y_perm"), _arg(s, y_q, torch.uint8, "y_q"),
+        _arg(s, y_scale, torch.float32, "y_scale"), _arg(s, dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -500,9 +553,10 @@ def moe_combine_fp8(shape, y_q, y_scale, dest_row, topk_w, y, stream=None):
     """Combine of e4m3 expert outputs with 128-column block scales."""
     s = _shape(shape)
     _check("moe_combine_fp8", load_library().moe_combine_fp8(
-        ctypes.byref(s), _ptr(y_q, torch.uint8, "y_q"), _ptr(y_scale, torch.float32, "y_scale"),
-        _ptr(dest_row, torch.int32, "dest_row"), _ptr(topk_w, torch.float32, "topk_w"),
-        _ptr(y, torch.bfloat16, "y"), _stream(stream)))
+        ctypes.byref(s), _arg(s, y_q, torch.uint8, "y_q"),
+        _arg(s, y_scale, torch.float32, "y_scale"),
+        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, y, torch.bfloat16, "y"), _stream(stream)))
 
 
 def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, topk_idx=None,
@@ -515,12 +569,13 @@ def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, top
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd_fp8", load_library().moe_layer_fwd_fp8(
-        ctypes.byref(s), _ptr(x, torch.bfloat16, "x"), _ptr(gate, torch.bfloat16, "gate"),
-        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(q.W1q, torch.uint8, "W1q"),
-        _ptr(q.w1_scale, torch.float32, "w1_scale"), _ptr(q.W2q, torch.uint8, "W2q"),
-        _ptr(q.w2_scale, torch.float32, "w2_scale"), _ptr(y, torch.bfloat16, "y"),
-        _ptr(aux, torch.float32, "aux"), _ptr(topk_idx, torch.int32, "topk_idx"),
-        _ptr(topk_w, torch.float32, "topk_w"), _ptr(routed_counts, torch.int32, "routed_counts"),
-        _ptr(P, torch.float32, "P"), _ptr(kept_counts, torch.int32, "kept_counts"),
-        _ptr(offsets, torch.int32, "offsets"), _ptr(dest_row, torch.int32, "dest_row"),
-        _ptr(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))
+        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
+        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, q.W1q, torch.uint8, "W1q"),
+        _arg(s, q.w1_scale, torch.float32, "w1_scale"), _arg(s, q.W2q, torch.uint8, "W2q"),
+        _arg(s, q.w2_scale, torch.float32, "w2_scale"), _arg(s, y, torch.bfloat16, "y"),
+        _arg(s, aux, torch.float32, "aux"), _arg(s, topk_idx, torch.int32, "topk_idx"),
+        _arg(s, topk_w, torch.float32, "topk_w"),
+        _arg(s, routed_counts, torch.int32, "routed_counts"),
+        _arg(s, P, torch.float32, "P"), _arg(s, kept_counts, torch.int32, "kept_counts"),
+        _arg(s, offsets, torch.int32, "offsets"), _arg(s, dest_row, torch.int32, "dest_row"),
+        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))
