@@ -226,8 +226,7 @@ def test_binding_sizes_every_tensor_argument():
     cannot check sizes), and the counts follow the header's layouts."""
     import inspect
     src = inspect.getsource(moe)
-    names = set(re.findall(r'_arg\([a-z_.]+, [A-Za-z0-9_.]+, torch\.[a-z0-9]+, "([A-Za-z0-9_]+)"\)',
-                           src))
+    names = set(re.findall(r'\ba\([A-Za-z0-9_.]+, torch\.[a-z0-9]+, "([A-Za-z0-9_]+)"\)', src))
     assert len(names) >= 30
     s = moe.MoeShape.make(1000, 384, 12, 3, 320, 1.0)
     A = 1000 * 3

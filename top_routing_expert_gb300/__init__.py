@@ -10,6 +10,7 @@ the dtypes below; outputs are written in place. A non-OK status raises
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Optional, Sequence
 
@@ -132,7 +133,7 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor", numel: Optional[i
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if t.device.index != torch.cuda.current_device():
+    if t.get_device() != torch.cuda.current_device():
         raise ValueError(f"{name} is on {t.device}, the current device is "
                          f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
@@ -147,7 +148,11 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor", numel: Optional[i
 def _need(s: "MoeShape", name: str) -> int:
     """Elements the named argument must hold for shape s (layouts as in
     include/moe_gb300.h)."""
-    T, H, E, k, h = s.T, s.H, s.E, s.top_k, s.h
+    return _need_table(s.T, s.H, s.E, s.top_k, s.h)[name]
+
+
+@functools.lru_cache(maxsize=64)
+def _need_table(T: int, H: int, E: int, k: int, h: int) -> dict:
     A = T * k
     return {
         "x": T * H, "y": T * H, "gate": H * E, "gate_bias": E, "noise_u": T * E,
@@ -159,11 +164,29 @@ def _need(s: "MoeShape", name: str) -> int:
         "x_scale": A, "y_scale": A * ((H + 127) // 128),
         "W1": E * H * h, "W2": E * h * H, "W1q": E * h * H, "W2q": E * H * h,
         "w1_scale": E * h, "w2_scale": E * H,
-    }[name]
+    }
 
 
-def _arg(s: "MoeShape", t: Optional[torch.Tensor], dtype, name: str) -> Optional[int]:
-    return _ptr(t, dtype, name, None if t is None else _need(s, name))
+class _Args:
+    """Argument checks of one shaped entry-point call: the shape, its size
+    table and the current device are looked up once, then each tensor is
+    checked as `_ptr` does (contiguous CUDA tensor of the dtype on the current
+    device, at least the elements the shape needs) and its address returned."""
+    __slots__ = ("shape", "need", "dev")
+
+    def __init__(self, shape):
+        self.shape = _shape(shape)
+        s = self.shape
+        self.need = _need_table(s.T, s.H, s.E, s.top_k, s.h)
+        self.dev = torch.cuda.current_device()
+
+    def __call__(self, t: Optional[torch.Tensor], dtype, name: str) -> Optional[int]:
+        if t is None:
+            return None
+        if not t.is_cuda or t.get_device() != self.dev or not t.is_contiguous() \
+                or t.dtype != dtype or t.numel() < self.need[name]:
+            return _ptr(t, dtype, name, self.need[name])   # raises with the reason
+        return t.data_ptr()
 
 
 def _stream(stream) -> Optional[int]:
@@ -245,95 +268,102 @@ def _events(events):
 def moe_route(shape, x, gate, gate_bias, topk_idx, topk_w, routed_counts=None, P=None,
               aux=None, logits_out=None, dev_status=None, ws: Workspace | None = None,
               stream=None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_route", load_library().moe_route(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
-        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"),
-        _arg(s, P, torch.float32, "P"), _arg(s, aux, torch.float32, "aux"),
-        _arg(s, logits_out, torch.float32, "logits_out"),
-        _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"), a(gate, torch.bfloat16, "gate"),
+        a(gate_bias, torch.float32, "gate_bias"), a(topk_idx, torch.int32, "topk_idx"),
+        a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"),
+        a(P, torch.float32, "P"), a(aux, torch.float32, "aux"),
+        a(logits_out, torch.float32, "logits_out"),
+        a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_route_logits(shape, logits, topk_idx, topk_w, routed_counts=None, P=None, aux=None,
                      dev_status=None, ws: Workspace | None = None, stream=None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_route_logits", load_library().moe_route_logits(
-        ctypes.byref(s), _arg(s, logits, torch.float32, "logits"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
-        _arg(s, aux, torch.float32, "aux"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(logits, torch.float32, "logits"),
+        a(topk_idx, torch.int32, "topk_idx"), a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"), a(P, torch.float32, "P"),
+        a(aux, torch.float32, "aux"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_permute(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x_perm,
                 dev_status=None, ws: Workspace | None = None, stream=None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_permute", load_library().moe_permute(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
-        _arg(s, x_perm, torch.bfloat16, "x_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"),
+        a(topk_idx, torch.int32, "topk_idx"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(src_token, torch.int32, "src_token"),
+        a(x_perm, torch.bfloat16, "x_perm"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_expert_ffn(shape, x_perm, offsets, W1, W2, act, y_perm, dev_status=None,
                    ws: Workspace | None = None, stream=None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn", load_library().moe_expert_ffn(
-        ctypes.byref(s), _arg(s, x_perm, torch.bfloat16, "x_perm"),
-        _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, W1, torch.bfloat16, "W1"), _arg(s, W2, torch.bfloat16, "W2"),
-        _arg(s, act, torch.bfloat16, "act"), _arg(s, y_perm, torch.bfloat16, "y_perm"),
-        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+        ctypes.byref(s), a(x_perm, torch.bfloat16, "x_perm"),
+        a(offsets, torch.int32, "offsets"),
+        a(W1, torch.bfloat16, "W1"), a(W2, torch.bfloat16, "W2"),
+        a(act, torch.bfloat16, "act"), a(y_perm, torch.bfloat16, "y_perm"),
+        a(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
 
 
 def moe_expert_ffn_gathered(shape, x, src_token, offsets, W1, W2, act, y_perm, dev_status=None,
                             ws: Workspace | None = None, stream=None):
     """moe_expert_ffn on x[src_token] without the permuted copy: GEMM1
     gathers its A rows from x by TMA."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn_gathered", load_library().moe_expert_ffn_gathered(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
-        _arg(s, src_token, torch.int32, "src_token"),
-        _arg(s, offsets, torch.int32, "offsets"), _arg(s, W1, torch.bfloat16, "W1"),
-        _arg(s, W2, torch.bfloat16, "W2"), _arg(s, act, torch.bfloat16, "act"),
-        _arg(s, y_perm, torch.bfloat16, "y_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"),
+        a(src_token, torch.int32, "src_token"),
+        a(offsets, torch.int32, "offsets"), a(W1, torch.bfloat16, "W1"),
+        a(W2, torch.bfloat16, "W2"), a(act, torch.bfloat16, "act"),
+        a(y_perm, torch.bfloat16, "y_perm"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_combine(shape, y_perm, dest_row, topk_w, y, stream=None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     _check("moe_combine", load_library().moe_combine(
-        ctypes.byref(s), _arg(s, y_perm, torch.bfloat16, "y_perm"),
-        _arg(s, dest_row, torch.int32, "dest_row"),
-        _arg(s, topk_w, torch.float32, "topk_w"), _arg(s, y, torch.bfloat16, "y"), _stream(stream)))
+        ctypes.byref(s), a(y_perm, torch.bfloat16, "y_perm"),
+        a(dest_row, torch.int32, "dest_row"),
+        a(topk_w, torch.float32, "topk_w"), a(y, torch.bfloat16, "y"), _stream(stream)))
 
 
 def moe_layer_fwd(shape, x, gate, gate_bias, W1, W2, y, aux=None, topk_idx=None, topk_w=None,
                   routed_counts=None, P=None, kept_counts=None, offsets=None, dest_row=None,
                   dev_status=None, ws: Workspace | None = None, stream=None,
                   events: Optional[Sequence[torch.cuda.Event]] = None):
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd", load_library().moe_layer_fwd(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
-        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, W1, torch.bfloat16, "W1"),
-        _arg(s, W2, torch.bfloat16, "W2"), _arg(s, y, torch.bfloat16, "y"),
-        _arg(s, aux, torch.float32, "aux"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
-        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"), a(gate, torch.bfloat16, "gate"),
+        a(gate_bias, torch.float32, "gate_bias"), a(W1, torch.bfloat16, "W1"),
+        a(W2, torch.bfloat16, "W2"), a(y, torch.bfloat16, "y"),
+        a(aux, torch.float32, "aux"),
+        a(topk_idx, torch.int32, "topk_idx"), a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"), a(P, torch.float32, "P"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
 
 
@@ -344,13 +374,14 @@ def moe_permute_noalloc(shape, x, topk_idx, kept_counts, offsets, dest_row, src_
     library (one per GPU). Larger shapes raise MoeError (unsupported).
     Calls that overlap on the GPU share that array and must be serialised;
     make the first call on a device before any stream capture."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
-        _arg(s, x_perm, torch.bfloat16, "x_perm"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"),
+        a(topk_idx, torch.int32, "topk_idx"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(src_token, torch.int32, "src_token"),
+        a(x_perm, torch.bfloat16, "x_perm"), a(dev_status, torch.int32, "dev_status"),
         _stream(stream)))
 
 
@@ -409,29 +440,30 @@ class HostPipeline:
             if aux_host.is_cuda or aux_host.dtype != torch.float32 or aux_host.numel() < n:
                 raise ValueError("aux_host must be a float32 host tensor with >= n entries")
             aux = aux_host.data_ptr()
+        a = _Args(self.shape)
         st = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
         ev = (ctypes.c_void_p * 6)(*[e.cuda_event for e in self.events])
         if self.fp8:
             q = W1  # an Fp8Weights
             _check("moe_layer_fwd_host_fp8", load_library().moe_layer_fwd_host_fp8(
                 ctypes.byref(self.shape), n, xs, ys, aux,
-                _arg(self.shape, gate, torch.bfloat16, "gate"),
-                _arg(self.shape, gate_bias, torch.float32, "gate_bias"),
-                _arg(self.shape, q.W1q, torch.uint8, "W1q"),
-                _arg(self.shape, q.w1_scale, torch.float32, "w1_scale"),
-                _arg(self.shape, q.W2q, torch.uint8, "W2q"),
-                _arg(self.shape, q.w2_scale, torch.float32, "w2_scale"),
-                _arg(self.shape, dev_status, torch.int32, "dev_status"), self.buf.data_ptr(),
+                a(gate, torch.bfloat16, "gate"),
+                a(gate_bias, torch.float32, "gate_bias"),
+                a(q.W1q, torch.uint8, "W1q"),
+                a(q.w1_scale, torch.float32, "w1_scale"),
+                a(q.W2q, torch.uint8, "W2q"),
+                a(q.w2_scale, torch.float32, "w2_scale"),
+                a(dev_status, torch.int32, "dev_status"), self.buf.data_ptr(),
                 self.nbytes,
                 st, ev))
             return self.streams[2]
         _check("moe_layer_fwd_host", load_library().moe_layer_fwd_host(
             ctypes.byref(self.shape), n, xs, ys, aux,
-            _arg(self.shape, gate, torch.bfloat16, "gate"),
-            _arg(self.shape, gate_bias, torch.float32, "gate_bias"),
-            _arg(self.shape, W1, torch.bfloat16, "W1"),
-            _arg(self.shape, W2, torch.bfloat16, "W2"),
-            _arg(self.shape, dev_status, torch.int32, "dev_status"),
+            a(gate, torch.bfloat16, "gate"),
+            a(gate_bias, torch.float32, "gate_bias"),
+            a(W1, torch.bfloat16, "W1"),
+            a(W2, torch.bfloat16, "W2"),
+            a(dev_status, torch.int32, "dev_status"),
             self.buf.data_ptr(), self.nbytes, st, ev))
         return self.streams[2]
 
@@ -454,17 +486,18 @@ def moe_route_gumbel(shape, x, gate, gate_bias, noise_u, temperature, topk_idx, 
                      routed_counts=None, P=None, aux=None, scores_out=None, dev_status=None,
                      ws: Workspace | None = None, stream=None):
     """Training router: top-k of (x.gate + bias + gumbel(noise_u)) / temperature."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_route_gumbel", load_library().moe_route_gumbel(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
-        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, noise_u, torch.float32, "noise_u"),
-        float(temperature), _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"),
-        _arg(s, P, torch.float32, "P"), _arg(s, aux, torch.float32, "aux"),
-        _arg(s, scores_out, torch.float32, "scores_out"),
-        _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"), a(gate, torch.bfloat16, "gate"),
+        a(gate_bias, torch.float32, "gate_bias"), a(noise_u, torch.float32, "noise_u"),
+        float(temperature), a(topk_idx, torch.int32, "topk_idx"),
+        a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"),
+        a(P, torch.float32, "P"), a(aux, torch.float32, "aux"),
+        a(scores_out, torch.float32, "scores_out"),
+        a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
@@ -473,18 +506,19 @@ def moe_layer_fwd_gumbel(shape, x, gate, gate_bias, noise_u, temperature, W1, W2
                          kept_counts=None, offsets=None, dest_row=None, dev_status=None,
                          ws: Workspace | None = None, stream=None, events=None):
     """moe_layer_fwd with the Gumbel training router."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd_gumbel", load_library().moe_layer_fwd_gumbel(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
-        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, noise_u, torch.float32, "noise_u"),
-        float(temperature), _arg(s, W1, torch.bfloat16, "W1"), _arg(s, W2, torch.bfloat16, "W2"),
-        _arg(s, y, torch.bfloat16, "y"), _arg(s, aux, torch.float32, "aux"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"), _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"), _arg(s, P, torch.float32, "P"),
-        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x, torch.bfloat16, "x"), a(gate, torch.bfloat16, "gate"),
+        a(gate_bias, torch.float32, "gate_bias"), a(noise_u, torch.float32, "noise_u"),
+        float(temperature), a(W1, torch.bfloat16, "W1"), a(W2, torch.bfloat16, "W2"),
+        a(y, torch.bfloat16, "y"), a(aux, torch.float32, "aux"),
+        a(topk_idx, torch.int32, "topk_idx"), a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"), a(P, torch.float32, "P"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream), ev))
 
 
@@ -519,15 +553,16 @@ class Fp8Weights:
 def moe_permute_fp8(shape, x, topk_idx, kept_counts, offsets, dest_row, src_token, x_q, x_scale,
                     dev_status=None, ws: Workspace | None = None, stream=None):
     """moe_permute with an e4m3 payload: x_q [T*k,H] uint8, x_scale [T*k] fp32."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_permute_fp8", load_library().moe_permute_fp8(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"),
-        _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, kept_counts, torch.int32, "kept_counts"), _arg(s, offsets, torch.int32, "offsets"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, src_token, torch.int32, "src_token"),
-        _arg(s, x_q, torch.uint8, "x_q"), _arg(s, x_scale, torch.float32, "x_scale"),
-        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+        ctypes.byref(s), a(x, torch.bfloat16, "x"),
+        a(topk_idx, torch.int32, "topk_idx"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(src_token, torch.int32, "src_token"),
+        a(x_q, torch.uint8, "x_q"), a(x_scale, torch.float32, "x_scale"),
+        a(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
 
 
 def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm=None,
@@ -536,27 +571,29 @@ def moe_expert_ffn_fp8(shape, x_q, x_scale, offsets, q: Fp8Weights, act, y_perm=
     """Expert FFN on e4m3 rows; outputs bf16 y_perm, or e4m3 y_q [T*k,H]
     (uint8) with y_scale [T*k, ceil(H/128)] block scales. ws must be an
     fp8=True workspace."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     _check("moe_expert_ffn_fp8", load_library().moe_expert_ffn_fp8(
-        ctypes.byref(s), _arg(s, x_q, torch.uint8, "x_q"),
-        _arg(s, x_scale, torch.float32, "x_scale"),
-        _arg(s, offsets, torch.int32, "offsets"), _arg(s, q.W1q, torch.uint8, "W1q"),
-        _arg(s, q.w1_scale, torch.float32, "w1_scale"), _arg(s, q.W2q, torch.uint8, "W2q"),
-        _arg(s, q.w2_scale, torch.float32, "w2_scale"), _arg(s, act, torch.bfloat16, "act"),
-        _arg(s, y_perm, torch.bfloat16, "y_perm"), _arg(s, y_q, torch.uint8, "y_q"),
-        _arg(s, y_scale, torch.float32, "y_scale"), _arg(s, dev_status, torch.int32, "dev_status"),
+        ctypes.byref(s), a(x_q, torch.uint8, "x_q"),
+        a(x_scale, torch.float32, "x_scale"),
+        a(offsets, torch.int32, "offsets"), a(q.W1q, torch.uint8, "W1q"),
+        a(q.w1_scale, torch.float32, "w1_scale"), a(q.W2q, torch.uint8, "W2q"),
+        a(q.w2_scale, torch.float32, "w2_scale"), a(act, torch.bfloat16, "act"),
+        a(y_perm, torch.bfloat16, "y_perm"), a(y_q, torch.uint8, "y_q"),
+        a(y_scale, torch.float32, "y_scale"), a(dev_status, torch.int32, "dev_status"),
         wp, wn, _stream(stream)))
 
 
 def moe_combine_fp8(shape, y_q, y_scale, dest_row, topk_w, y, stream=None):
     """Combine of e4m3 expert outputs with 128-column block scales."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     _check("moe_combine_fp8", load_library().moe_combine_fp8(
-        ctypes.byref(s), _arg(s, y_q, torch.uint8, "y_q"),
-        _arg(s, y_scale, torch.float32, "y_scale"),
-        _arg(s, dest_row, torch.int32, "dest_row"), _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, y, torch.bfloat16, "y"), _stream(stream)))
+        ctypes.byref(s), a(y_q, torch.uint8, "y_q"),
+        a(y_scale, torch.float32, "y_scale"),
+        a(dest_row, torch.int32, "dest_row"), a(topk_w, torch.float32, "topk_w"),
+        a(y, torch.bfloat16, "y"), _stream(stream)))
 
 
 def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, topk_idx=None,
@@ -565,17 +602,18 @@ def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, top
                       events=None):
     """moe_layer_fwd with the FP8 dispatch and expert FFN; ws must be an
     fp8=True workspace."""
-    s = _shape(shape)
+    a = _Args(shape)
+    s = a.shape
     wp, wn = _ws(ws, s)
     ev = _events(events)
     _check("moe_layer_fwd_fp8", load_library().moe_layer_fwd_fp8(
-        ctypes.byref(s), _arg(s, x, torch.bfloat16, "x"), _arg(s, gate, torch.bfloat16, "gate"),
-        _arg(s, gate_bias, torch.float32, "gate_bias"), _arg(s, q.W1q, torch.uint8, "W1q"),
-        _arg(s, q.w1_scale, torch.float32, "w1_scale"), _arg(s, q.W2q, torch.uint8, "W2q"),
-        _arg(s, q.w2_scale, torch.float32, "w2_scale"), _arg(s, y, torch.bfloat16, "y"),
-        _arg(s, aux, torch.float32, "aux"), _arg(s, topk_idx, torch.int32, "topk_idx"),
-        _arg(s, topk_w, torch.float32, "topk_w"),
-        _arg(s, routed_counts, torch.int32, "routed_counts"),
-        _arg(s, P, torch.float32, "P"), _arg(s, kept_counts, torch.int32, "kept_counts"),
-        _arg(s, offsets, torch.int32, "offsets"), _arg(s, dest_row, torch.int32, "dest_row"),
-        _arg(s, dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))
+        ctypes.byref(s), a(x, torch.bfloat16, "x"), a(gate, torch.bfloat16, "gate"),
+        a(gate_bias, torch.float32, "gate_bias"), a(q.W1q, torch.uint8, "W1q"),
+        a(q.w1_scale, torch.float32, "w1_scale"), a(q.W2q, torch.uint8, "W2q"),
+        a(q.w2_scale, torch.float32, "w2_scale"), a(y, torch.bfloat16, "y"),
+        a(aux, torch.float32, "aux"), a(topk_idx, torch.int32, "topk_idx"),
+        a(topk_w, torch.float32, "topk_w"),
+        a(routed_counts, torch.int32, "routed_counts"),
+        a(P, torch.float32, "P"), a(kept_counts, torch.int32, "kept_counts"),
+        a(offsets, torch.int32, "offsets"), a(dest_row, torch.int32, "dest_row"),
+        a(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))
