@@ -382,6 +382,73 @@ def test_all_experts_layer_is_a_soft_mixture():
     assert np.mean(out.y == ref) > 0.9
 
 
+def _partial_drop_case():
+    """40 tokens, 3 experts, top-2, cf = 1 (C = ceil(80/3) = 27). The gate and
+    bias give logits (1.0, 0.5, 0.5 + x[t,0]/8), so every token takes expert
+    0 first and expert 1 or 2 (by the sign of x[t,0]) second: expert 0 is
+    asked by all 40 tokens and serves tokens 0..26 only, experts 1 and 2 are
+    asked by about 20 each and serve them all. Tokens 27..39 therefore keep
+    their second slot and lose their first."""
+    g = np.random.default_rng(77)
+    T, H, E, k, h, cf = 40, 64, 3, 2, 64, 1.0
+    x = O.bf16_round(g.standard_normal((T, H)))
+    gate = np.zeros((H, E))
+    gate[0, 2] = 0.125
+    bias = np.array([1.0, 0.5, 0.5], np.float32)
+    W1 = O.bf16_round(g.standard_normal((E, H, h)) / 8)
+    W2 = O.bf16_round(g.standard_normal((E, h, H)) / 8)
+    return x, gate, bias, W1, W2, k, cf
+
+
+def test_partial_drop_keeps_the_surviving_weight_unrenormalised():
+    # The pages drop assignments past capacity (comm bottleneck 3.1) into a
+    # combine buffer that starts at zero (module notes 4.2, _scatter_back);
+    # nothing rescales the survivors, so a token that keeps one slot of two
+    # outputs w_kept * FFN_e(x) with w_kept < 1.
+    x, gate, bias, W1, W2, k, cf = _partial_drop_case()
+    T, E = x.shape[0], gate.shape[1]
+    C = 27
+    out = O.layer_forward(x, gate, bias, W1, W2, k, cf)
+    # routing and drops from the closed-form structure of the case
+    second = np.where(x[:, 0] > 0, 2, 1)
+    assert (np.sort(out.routing.idx, axis=1) == np.stack([np.zeros(T, int), second], 1)).all()
+    assert max((second == 1).sum(), (second == 2).sum()) <= C
+    kept = np.ones((T, k), bool)
+    slot0 = np.argmax(out.routing.idx == 0, axis=1)          # the slot naming expert 0
+    kept[np.arange(T)[C:], slot0[C:]] = False
+    assert np.array_equal(out.dispatch.dest_row >= 0, kept)
+    assert (kept.sum(1) == 1).sum() == T - C
+    # expected outputs by torch ops in float64: weights from the softmax of
+    # the logits renormalised over the chosen two, one expert FFN per slot,
+    # only the kept slots summed, in slot order
+    lg = torch.from_numpy(out.logits.astype(np.float64))
+    p = torch.softmax(lg, dim=1)
+    idx = torch.from_numpy(out.routing.idx.astype(np.int64))
+    pk = torch.gather(p, 1, idx)
+    w = pk / pk.sum(1, keepdim=True)
+    xt = torch.from_numpy(x)
+    ffn = []
+    for e in range(E):
+        act = _torch_bf16(torch.nn.functional.gelu(xt @ torch.from_numpy(W1[e]), approximate="tanh"))
+        ffn.append(_torch_bf16(act @ torch.from_numpy(W2[e])))
+    acc = torch.zeros_like(xt)
+    renorm = torch.zeros_like(xt)
+    for t in range(T):
+        wk = [float(w[t, j]) for j in range(k) if kept[t, j]]
+        for j in range(k):
+            if kept[t, j]:
+                acc[t] += w[t, j] * ffn[int(idx[t, j])][t]
+                renorm[t] += w[t, j] / sum(wk) * ffn[int(idx[t, j])][t]
+    ref = _torch_bf16(acc).numpy()
+    assert np.allclose(out.y, ref, rtol=2.0 ** -5, atol=1e-3 * np.abs(ref).max())
+    assert np.mean(out.y == ref) > 0.9
+    # the rescaled alternative differs by the factor 1/w_kept on those tokens
+    alt = _torch_bf16(renorm).numpy()
+    part = np.arange(C, T)
+    assert not np.allclose(out.y[part], alt[part], rtol=0.05, atol=1e-3 * np.abs(alt).max())
+    assert (w.numpy()[part][~kept[part]] > 0.1).all()
+
+
 def test_token_outputs_equal_layer_rows():
     T, H, E, k, h = 60, 64, 6, 2, 64
     x = O.bf16_round(rng.standard_normal((T, H)))
@@ -452,6 +519,17 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(O, "dispatch_plan", slot_major)
     with pytest.raises(AssertionError):
         test_dispatch_hand_example()
+    monkeypatch.undo()
+    # surviving weights rescaled to sum to 1 after a drop
+    real_combine = O.combine
+
+    def renormalising(y_perm, d, w, H):
+        kw = np.where(d.dest_row >= 0, w, 0.0)
+        s = kw.sum(axis=1, keepdims=True)
+        return real_combine(y_perm, d, np.where(s > 0, kw / np.where(s > 0, s, 1.0), 0.0), H)
+    monkeypatch.setattr(O, "combine", renormalising)
+    with pytest.raises(AssertionError):
+        test_partial_drop_keeps_the_surviving_weight_unrenormalised()
     monkeypatch.undo()
 
 
