@@ -12,8 +12,9 @@ import torch
 import top_routing_expert_gb300 as moe
 import workloads as W
 from oracle import moe_oracle as O
-from tests._helpers import (NEAR_TIE, assert_ffn_close, assert_fp8_out_close, fill_nan_bf16, np64,
-                            oracle_logits_chunked, topk_margins)
+from tests._helpers import (NEAR_TIE, assert_dispatch_on_gpu_indices, assert_ffn_close,
+                            assert_fp8_out_close, fill_nan_bf16, np64, oracle_logits_chunked,
+                            routing_flips, topk_margins)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -255,12 +256,11 @@ def _check_layer_fp8(w, inp, g, Q, sample=None, check_experts=None):
     r = O.route_from_logits(lg, k)
     d = O.dispatch_plan(r.idx, E, O.capacity(T, E, k, w.cf))
     gidx = g["topk_idx"].numpy()
-    mism = np.nonzero((gidx != r.idx).any(axis=1))[0]
-    assert (topk_margins(lg, k)[mism] < NEAR_TIE).all()
+    routing_flips(gidx, r.idx, topk_margins(lg, k), f"{w.name} fp8")
     gdest = g["dest_row"].numpy()
-    if len(mism) == 0:
-        assert np.array_equal(g["offsets"].numpy(), d.offsets)
-        assert np.array_equal(gdest, d.dest_row)
+    assert_dispatch_on_gpu_indices(gidx, r.p, E, O.capacity(T, E, k, w.cf),
+                                   offsets=g["offsets"].numpy(), dest_row=gdest,
+                                   aux=float(g["aux"].item()))
     for e in (range(E) if check_experts is None else check_experts):
         q1, s1 = O.quantize_weights_fp8(np64(inp["W1"][e]))
         assert np.array_equal(e4m3_values(Q.W1q[e]), q1)
@@ -422,7 +422,8 @@ def test_combine_fp8_against_oracle(T, H, k, drop):
 def test_layer_fp8_host_pipeline_equals_device_layer():
     """moe_layer_fwd_host_fp8 over three micro-batches (copies overlapped with
     the FP8 layer on three streams) gives each micro-batch's
-    moe_layer_fwd_fp8 output bit for bit."""
+    moe_layer_fwd_fp8 output bit for bit, and each micro-batch's y matches
+    the oracle's FP8 layer."""
     w = W.custom(1000, 256, 12, 3, 320, 1.0, "zipf", name="pipe8")
     shape = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
     base = W.make_inputs(w, seed=31)
@@ -441,10 +442,21 @@ def test_layer_fp8_host_pipeline_equals_device_layer():
     for i, x in enumerate(xs):
         y = _zeros((w.T, w.H), torch.bfloat16)
         aux = _zeros(1, torch.float32)
-        moe.moe_layer_fwd_fp8(shape, x.to(DEV), gate, bias, Q, y, aux=aux, ws=ws)
+        idx = _zeros((w.T, w.k), torch.int32)
+        moe.moe_layer_fwd_fp8(shape, x.to(DEV), gate, bias, Q, y, aux=aux, topk_idx=idx, ws=ws)
         torch.cuda.synchronize()
         assert torch.equal(y.cpu(), y_host[i]), i
         assert float(aux.item()) == float(aux_host[i])
+        # each micro-batch's y against the oracle's FP8 layer on the GPU's
+        # own indices (flips only on near-ties)
+        gidx = idx.cpu().numpy()
+        lg = oracle_logits_chunked(x, base["gate"], base["bias"])
+        r = O.route_from_logits(lg, w.k)
+        routing_flips(gidx, r.idx, topk_margins(lg, w.k), f"fp8 host pipeline {i}")
+        d = O.dispatch_plan(gidx, w.E, O.capacity(w.T, w.E, w.k, w.cf))
+        ref = O.token_outputs_fp8(np64(x), gidx, O.renormalise(r.p, gidx), d.dest_row >= 0,
+                                  _LazyQ(base["W1"]), _LazyQ(base["W2"]), fp8_combine=True)
+        assert_fp8_out_close(np64(y_host[i]), ref, f"fp8 host pipeline micro-batch {i}")
 
 
 def test_layer_fp8_captured_in_a_cuda_graph():
