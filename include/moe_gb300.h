@@ -345,13 +345,16 @@ MOE_API moe_status moe_layer_fwd_host_fp8(const moe_shape* s, int64_t n_micro,
  * have no counterpart to this entry point; it serves code that may not call
  * cudaMalloc or hold a workspace: a plugin inside a runtime that owns all
  * device memory, or code issuing work while a stream is being captured.
- * Same arguments and results as moe_permute, minus ws/ws_bytes: the scratch
- * is one static 1 MiB device array per GPU, held until the process exits.
- *   - Shapes whose scratch exceeds 1 MiB (2 * E * ceil(T/128) * 4 bytes of
- *     tile counters plus T*k rank bytes, each rounded up to 256, plus 1 KiB)
- *     return MOE_ERR_UNSUPPORTED before any launch.
- *   - The first call on a device looks the array's address up (once per
- *     device); make it before any stream capture.
+ * Same arguments and results as moe_permute, minus ws/ws_bytes (x_perm may
+ * be NULL when src_token is given): the scratch is one static 1 MiB device
+ * array per GPU, held until the process exits.
+ *   - Shapes whose scratch exceeds 1 MiB return MOE_ERR_UNSUPPORTED before
+ *     any launch. The scratch is 2*r(4*E*ceil(T/128)) + r(T*k) + 2*r(4*E)
+ *     + 512 bytes, r() rounding up to a multiple of 256 (tile counts and
+ *     bases, in-tile ranks, per-expert counts and sums, ticket and status).
+ *   - The first call in a CUDA context looks the array's address up (again
+ *     after the context is torn down and made anew, e.g. by
+ *     cudaDeviceReset); make it before any stream capture.
  *   - All calls on a device share the array; calls that overlap on the GPU
  *     race and must be serialised by the caller. Allocates nothing. */
 MOE_API moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x, const int32_t* topk_idx,

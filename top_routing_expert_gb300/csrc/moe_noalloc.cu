@@ -14,8 +14,11 @@
 //     library, held until the process exits.
 //   - Shapes whose scratch does not fit are rejected with
 //     MOE_ERR_UNSUPPORTED before anything is launched.
-//   - The first call on a device looks up the array's device address (once
-//     per device); make that first call before any stream capture.
+//   - The first call in a CUDA context looks up the array's device address
+//     (once per device and context: a context torn down and made again, as
+//     by cudaDeviceReset, reloads the library's module and moves the array,
+//     so the address is looked up again); make that first call before any
+//     stream capture.
 //   - Every call on a device shares the one array and leaves its contents
 //     behind. What must start at zero (the scan ticket) is cleared by the
 //     call's own first kernel; calls that overlap on the GPU (two streams,
@@ -37,18 +40,54 @@ static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticScratch
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_dispatch_scratch for the current device, looked up
-// once per device with that device current. nullptr on failure.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Process-unique id of the current CUDA context (0 if there is none yet),
+// through the driver entry points the runtime hands out. false if the
+// driver offers no context ids.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_dispatch_scratch in the current device's current
+// context, looked up with that device current the first time a context is
+// seen and again whenever the device's context has changed (a reset context
+// holds a new copy of the array). nullptr on failure.
 unsigned char* scratch_for_current_device() {
   static std::mutex mu;
   static unsigned char* addr[kMaxDevices] = {nullptr};
+  static unsigned long long ctx_of[kMaxDevices] = {0};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || id == 0 || ctx_of[dev] != id) {
     void* p = nullptr;
+    // makes the device's primary context current if nothing has yet
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess) return nullptr;
+    if (!current_context_id(&id) || id == 0) return nullptr;
     addr[dev] = static_cast<unsigned char*>(p);
+    ctx_of[dev] = id;
   }
   return addr[dev];
 }
@@ -67,8 +106,10 @@ extern "C" moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x,
   size_t unused = 0;
   const moe_status shape_ok = moe_workspace_size(s, &unused);  // the same shape checks
   if (shape_ok != MOE_OK) return shape_ok;
+  // as moe_permute: x_perm may be NULL when src_token is given (the
+  // permutation only)
   if (x == nullptr || topk_idx == nullptr || offsets == nullptr || dest_row == nullptr ||
-      x_perm == nullptr)
+      (x_perm == nullptr && src_token == nullptr))
     return MOE_ERR_NULL;
   const void* ptrs[] = {x, topk_idx, kept_counts, offsets, dest_row, src_token, x_perm, dev_status};
   for (const void* p : ptrs)
@@ -78,6 +119,8 @@ extern "C" moe_status moe_permute_noalloc(const moe_shape* s, const moe_bf16* x,
             k = static_cast<int>(s->top_k);
   const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
   const size_t tiles_bytes = round256(static_cast<size_t>(E) * n_tiles * 4);
+  // tile counts and tile bases, in-tile ranks, routed counts and P, the
+  // scan ticket and a status word (the same pieces `take` carves below)
   const size_t need = 2 * tiles_bytes + round256(static_cast<size_t>(T) * k) +
                       2 * round256(static_cast<size_t>(E) * 4) + 2 * 256;
   if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
