@@ -103,9 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + nst;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xbar = drain + 1;  // leader: the peer's count of loaded stages has arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 1);
   uint32_t* abort_flag = tmem_slot + 1;
-  int* offs = reinterpret_cast<int*>(abort_flag + 2);  // [E+1]
+  uint32_t* peer_issued = abort_flag + 1;              // leader: stages the peer loaded
+  int* offs = reinterpret_cast<int*>(peer_issued + 1);  // [E+1]
   int* pm_prefix = offs + (p.E + 1);                    // [E+1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], 2 * kEpiWarps * 32);  // both CTAs' epilogue threads
     }
     mbar_init(drain, 1);
+    mbar_init(xbar, 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -172,6 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = total_pm * n_tiles_n;
   const int nk = (p.K + kKE - 1) / kKE;  // a partial last block reads zeros past K
   const WaitCtl wc{abort_flag, p.dev_status, p.timeout_ns};
+  // A wait that gives up stops the peer CTA too: its waits see the raised
+  // flag within a few polls, so the pair aborts together.
+  const uint32_t peer_abort = mapa_shared(smem_u32(abort_flag), rank ^ 1u);
+  auto pair_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_wait(bar, parity, wc)) return true;
+    st_u32_cluster(peer_abort, 1u);
+    return false;
+  };
 
   if (warp == 0) {
     // lanes 1-31 leave at once unless they gather (they must not fall
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int kb = 0; kb < nk; ++kb) {
           bool ok = true;
-          if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, wc);
+          if (lane == 0) ok = pair_wait(&empty[stage], phase ^ 1u);
           if constexpr (kGather) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) {
             aborted = true;
@@ -232,25 +243,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (aborted && lane == 0) {
-        if (leader) {
-          // let the last loads issued land before the CTA exits (the leader's
-          // barriers count both CTAs' bytes)
-          int s = stage;
-          uint32_t ph = phase;
-          for (int d = 0; d < nst && d < issued; ++d) {
-            if (--s < 0) {
-              s = nst - 1;
-              ph ^= 1u;
-            }
-            mbar_wait_drain(&full[s], ph, kDrainLimitNs);
-          }
+      // Every load either CTA issued lands before either CTA can exit (the
+      // kernel ends with a cluster barrier, which the leader reaches only
+      // after this drain). Both CTAs' loads count their bytes on the
+      // leader's barriers, and after an abort the leader may not have armed
+      // a stage the peer loaded into, or armed one the peer never loaded:
+      // so the peer reports how many stages it loaded, and the leader makes
+      // the accounting of each stage still in flight whole before waiting
+      // for it. Stages more than a ring behind the last one issued were
+      // consumed by the UMMA, so they have landed.
+      if constexpr (kGather) __syncwarp();
+      if (lane == 0) {
+        if (!leader) {
+          st_async_u32_cluster(mapa_shared(smem_u32(peer_issued), 0),
+                               static_cast<uint32_t>(issued), mapa_shared(smem_u32(xbar), 0));
         } else {
-          // the peer's loads signal the leader's barriers, which may never
-          // be armed after an abort: give them a fixed grace period (a TMA
-          // tile lands within microseconds) before the CTA can exit
-          const uint64_t t0 = global_timer_ns();
-          while (global_timer_ns() - t0 < 1000000ull) {
+          mbar_arrive_expect_tx(xbar, 4);
+          int theirs = issued;
+          if (mbar_wait_drain(xbar, 0, p.timeout_ns + kDrainLimitNs)) {
+            // the peer cannot load more than a ring ahead of what this CTA armed
+            theirs = min(static_cast<int>(*reinterpret_cast<volatile uint32_t*>(peer_issued)),
+                         issued + nst);
+          } else {
+            atomicOr(p.dev_status, MOE_DEV_TIMEOUT);
+          }
+          const int hi = max(issued, theirs);
+          for (int i = max(0, hi - nst); i < hi; ++i) {
+            uint64_t* b = &full[i % nst];
+            if (i >= issued)
+              mbar_arrive_expect_tx(b, kStageBytes);  // armed here for the peer's half alone
+            else if (i >= theirs)
+              mbar_complete_tx(b, kStageBytes);       // the peer's half will never come
+            mbar_wait_drain(b, static_cast<uint32_t>(i / nst) & 1u, kDrainLimitNs);
           }
         }
       }
@@ -266,11 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool aborted = false;
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
+        if (!pair_wait(&tempty[acc], acc_phase ^ 1u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], phase, wc)) {
+          if (!pair_wait(&full[stage], phase)) {
             aborted = true;
             break;
           }
@@ -340,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) rs = p.a_scale[row];
         __syncwarp();
       }
-      if (!mbar_wait(&tfull[acc], acc_phase, wc)) break;
+      if (!pair_wait(&tfull[acc], acc_phase)) break;
       tc_fence_after();
       uint16_t* drow = p.D + static_cast<size_t>(valid ? row : 0) * p.N;
       float row_max = 0.f;  // FP8 mode: max |output| of this row in these columns
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t gemm_pair_smem_bytes(int E, int stages, bool fp8) {
   return 1024 + static_cast<size_t>(stages) * kStageBytes + (fp8 ? 4 * kEpiWarps * (kBN / 2) : 0) +
-         8 * (2 * stages + 5) + 16 + 8 * static_cast<size_t>(E + 1);
+         8 * (2 * stages + 6) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
 template <bool kFp8, bool kQOut, bool kGather>

@@ -277,6 +277,32 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Writes a 32-bit value into shared memory of a CTA of the cluster (by its
+// shared::cluster address) and counts its 4 bytes as completed transaction
+// bytes on an mbarrier of that same CTA: once the waiter sees the phase
+// complete, the value is there.
+__device__ __forceinline__ void st_async_u32_cluster(uint32_t cluster_addr, uint32_t value,
+                                                     uint32_t mbar_cluster_addr) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(value), "r"(mbar_cluster_addr)
+      : "memory");
+}
+
+// Plain 32-bit store into shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_u32_cluster(uint32_t cluster_addr, uint32_t value) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(value) : "memory");
+}
+
+// Counts `bytes` as completed transaction bytes on this CTA's mbarrier, as if
+// a copy of that size had landed (accounts for a copy that will never be
+// issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // TMA tile load into this CTA's shared memory whose transaction bytes are
 // counted on an mbarrier that may live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
