@@ -156,9 +156,15 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
       if (bits) atomicOr(a.dev_status, bits);
     }
     int d[kMaxTopK];
+    bool any = false;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) d[j] = __shfl_sync(0xffffffffu, dest, j);
-    if (pv == nullptr) continue;  // index-only dispatch: GEMM1 gathers the rows itself
+    for (int j = 0; j < kMaxTopK; ++j) {
+      d[j] = __shfl_sync(0xffffffffu, dest, j);
+      any |= j < a.k && d[j] >= 0;
+    }
+    // index-only dispatch (GEMM1 gathers the rows itself), or a token whose
+    // every slot was dropped: its row is not read at all
+    if (pv == nullptr || !any) continue;
 
     const uint4* src = xv + static_cast<size_t>(t) * nvec;
     for (int b = 0; b < nvec; b += 32 * U) {
