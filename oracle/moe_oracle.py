@@ -216,7 +216,7 @@ class Dispatch:
     N: int                 # kept assignments
 
 
-def dispatch_plan(idx: np.ndarray, E: int, C: int) -> Dispatch:
+def dispatch_plan(idx: np.ndarray, E: int, C) -> Dispatch:
     """Capacity-bounded, token-ordered dispatch (R6).
 
     Expert e serves its assignments in token order; the one at arrival
@@ -225,7 +225,8 @@ def dispatch_plan(idx: np.ndarray, E: int, C: int) -> Dispatch:
     which is the on-device stand-in for the dispatch all-to-all of comm
     bottleneck 1.1 (tokens grouped by destination expert). A token names an
     expert at most once, so ordering the flattened (t, j) list by expert with
-    a stable sort orders each expert's list by token.
+    a stable sort orders each expert's list by token. C may also be given
+    per expert (an array [E]; see ep_dispatch_plan).
     """
     T, k = idx.shape
     flat = idx.reshape(-1).astype(np.int64)
@@ -235,9 +236,10 @@ def dispatch_plan(idx: np.ndarray, E: int, C: int) -> Dispatch:
     pos_sorted = np.arange(flat.size, dtype=np.int64) - first[flat[order]]
     pos = np.empty(flat.size, dtype=np.int64)
     pos[order] = pos_sorted
-    kept_counts = np.minimum(routed, C)
+    cap = np.broadcast_to(np.asarray(C, np.int64), (E,))
+    kept_counts = np.minimum(routed, cap)
     offsets = np.concatenate([[0], np.cumsum(kept_counts)]).astype(np.int64)
-    kept = pos < C
+    kept = pos < cap[flat]
     dest = np.where(kept, offsets[flat] + pos, -1).astype(np.int32)
     N = int(offsets[-1])
     src = np.full(N, -1, dtype=np.int32)
@@ -246,6 +248,35 @@ def dispatch_plan(idx: np.ndarray, E: int, C: int) -> Dispatch:
     return Dispatch(C=C, pos=pos.reshape(T, k), kept_counts=kept_counts,
                     offsets=offsets, dest_row=dest.reshape(T, k),
                     src_token=src, N=N)
+
+
+def ep_dispatch_plan(idx: np.ndarray, E: int, C: int,
+                     routed_before: np.ndarray | None = None) -> Dispatch:
+    """One rank's dispatch when the experts live on different ranks (expert
+    parallelism: comm bottleneck 1.1 sends each token to the rank holding its
+    expert; module notes 4.2, ``_all_to_all_routed``).
+
+    With ``routed_before`` (per expert, how many assignments the ranks that
+    come before this one in the global token order made to it), each expert
+    serves the whole group's tokens in that global order, rank after rank:
+    this rank keeps its assignment at local position pos iff
+    routed_before[e] + pos < C, with C the capacity of the group's batch.
+    Without it, the rank applies C (then its own batch's capacity) to its own
+    tokens alone, as the module notes' listing does (its capacity comes from
+    the local batch). The rows are laid out expert-major as dispatch_plan
+    does; experts of one destination rank are contiguous."""
+    if routed_before is None:
+        return dispatch_plan(idx, E, C)
+    before = np.asarray(routed_before, np.int64)
+    return dispatch_plan(idx, E, np.maximum(C - before, 0))
+
+
+def ep_send_counts(kept_counts: np.ndarray, world: int) -> np.ndarray:
+    """Rows one rank sends to each rank: the kept rows of the E/world
+    consecutive experts that rank holds (rank g holds experts
+    g*E/world .. (g+1)*E/world - 1)."""
+    kc = np.asarray(kept_counts, np.int64)
+    return kc.reshape(world, -1).sum(axis=1)
 
 
 def permute(x: np.ndarray, d: Dispatch) -> np.ndarray:

@@ -297,6 +297,56 @@ def test_dispatch_matches_sequential_simulation(T, E, k, cf, skew):
     assert all(tuple(by_row[i]) < tuple(by_row[i + 1]) for i in range(len(by_row) - 1))
 
 
+@pytest.mark.parametrize("world,T,E,k,cf,skew", [
+    (2, 97, 12, 3, 0.9, 0.2), (3, 64, 6, 2, 0.5, 0.0), (4, 200, 16, 2, 1.0, 0.4),
+    (2, 33, 8, 8, 0.3, 0.0), (8, 57, 8, 1, 2.0, 1.0)])
+def test_ep_dispatch_in_global_order_is_the_unsharded_dispatch(world, T, E, k, cf, skew):
+    """Experts spread over `world` ranks, tokens split into contiguous shards:
+    with each expert serving the group's tokens in global order, every
+    rank's kept decisions and expert-major rows, regrouped on the rank that
+    holds the expert, must be exactly the single-device dispatch (sequential
+    per-expert counters over all tokens, the same simulation that pins
+    dispatch_plan)."""
+    idx = _random_idx(T, E, k, skew)
+    C = O.capacity(T, E, k, cf)
+    pos, kc, off, dest = _dispatch_brute(idx, E, C)
+    shards = np.array_split(np.arange(T), world)
+    E_loc = E // world
+    before = np.zeros(E, np.int64)
+    sent = []   # per source rank: its expert-major kept (token, expert) rows
+    for r, sh in enumerate(shards):
+        d = O.ep_dispatch_plan(idx[sh], E, C, before)
+        # kept decisions equal the unsharded ones
+        assert np.array_equal(d.dest_row >= 0, dest[sh] >= 0), r
+        assert np.array_equal(O.ep_send_counts(d.kept_counts, world),
+                              d.kept_counts.reshape(world, E_loc).sum(1))
+        # the rank's expert-major buffer as (expert, global token) per row
+        expert_of_row = np.repeat(np.arange(E), d.kept_counts)
+        sent.append([(int(e), int(sh[t])) for e, t in zip(expert_of_row, d.src_token)])
+        before += np.bincount(idx[sh].reshape(-1), minlength=E)
+    # rank g receives, from each source in rank order, that source's rows of
+    # its experts; regrouped expert-major (sources ascending inside an expert)
+    # they are the unsharded buffer's segments of those experts
+    unsharded = sorted((int(idx[t, j]), t) for t, j in zip(*np.nonzero(dest >= 0)))
+    for g in range(world):
+        mine = set(range(g * E_loc, (g + 1) * E_loc))
+        got = [et for src in sent for et in src if et[0] in mine]
+        regrouped = [et for e in sorted(mine) for et in got if et[0] == e]
+        assert regrouped == [et for et in unsharded if et[0] in mine], g
+
+
+def test_ep_dispatch_per_rank_capacity_is_the_local_dispatch():
+    """Without the other ranks' counts a rank applies its own batch's
+    capacity to its own tokens (the module notes' listing): the sequential
+    simulation on the shard alone."""
+    idx = _random_idx(80, 8, 2, 0.5)
+    sh = np.arange(40, 80)
+    C = O.capacity(len(sh), 8, 2, 1.0)
+    d = O.ep_dispatch_plan(idx[sh], 8, C)
+    pos, kc, off, dest = _dispatch_brute(idx[sh], 8, C)
+    assert np.array_equal(d.dest_row, dest) and np.array_equal(d.kept_counts, kc)
+
+
 def test_dispatch_hand_example():
     # 6 tokens, 4 experts, top-2, cf = 0.75 -> C = ceil(0.75*12/4) = 3
     idx = np.array([[0, 1], [1, 0], [2, 0], [0, 3], [1, 2], [3, 1]], np.int32)
@@ -530,6 +580,12 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(O, "combine", renormalising)
     with pytest.raises(AssertionError):
         test_partial_drop_keeps_the_surviving_weight_unrenormalised()
+    monkeypatch.undo()
+    # expert-parallel ranks that ignore the earlier ranks' claims on capacity
+    real_ep = O.ep_dispatch_plan
+    monkeypatch.setattr(O, "ep_dispatch_plan", lambda idx, E, C, before=None: real_ep(idx, E, C))
+    with pytest.raises(AssertionError):
+        test_ep_dispatch_in_global_order_is_the_unsharded_dispatch(2, 97, 12, 3, 0.9, 0.2)
     monkeypatch.undo()
 
 
