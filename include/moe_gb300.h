@@ -256,6 +256,39 @@ MOE_API moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const
                               uint32_t* dev_status, void* ws, size_t ws_bytes,
                               void* const* streams, void* const* events);
 
+/* Bytes of device workspace moe_layer_fwd_pipelined needs: two layer
+ * workspaces, used by alternate micro-batches. Host only. */
+MOE_API moe_status moe_pipelined_workspace_size(const moe_shape* s, size_t* bytes);
+
+/* The layer forward over n_micro micro-batches of s->T tokens each, on the
+ * device, pipelined over two caller streams - the dual-stream, micro-batch
+ * overlap of the MoE comm bottleneck page, section 5.2, with the on-device
+ * dispatch and combine in the role of the all-to-alls: while micro-batch i
+ * runs its two expert GEMMs on streams[1], streams[0] routes and permutes
+ * micro-batch i+1 and combines micro-batch i-1, so those memory-bound
+ * kernels run beside the GEMMs on the SM resources the GEMM leaves free.
+ *   x [n_micro*T, H], y [n_micro*T, H] bf16 (device): micro-batch i is rows
+ *        i*T .. i*T+T-1; each micro-batch is a layer forward of its own
+ *        (its own routing, capacity and statistics), with the outputs of
+ *        moe_layer_fwd on those rows.
+ *   aux [n_micro] fp32 (device) or NULL: each micro-batch's aux.
+ *   gate, gate_bias (nullable), W1, W2, dev_status (nullable): as moe_layer_fwd.
+ *   ws: >= moe_pipelined_workspace_size bytes.
+ *   streams: host array of 2 cudaStream_t (dispatch, expert), distinct and
+ *        not the legacy default stream; give the dispatch stream the higher
+ *        priority (cudaStreamCreateWithPriority) so that its kernels are
+ *        scheduled as soon as resources free up.
+ *   events: host array of 4 cudaEvent_t created by the caller (timing may be
+ *        disabled); they order the two streams.
+ * Everything is enqueued and the call returns; y and aux are complete once
+ * streams[0] has completed (its last kernel is the last combine). */
+MOE_API moe_status moe_layer_fwd_pipelined(const moe_shape* s, int64_t n_micro, const moe_bf16* x,
+                                           const moe_bf16* gate, const float* gate_bias,
+                                           const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y,
+                                           float* aux, uint32_t* dev_status, void* ws,
+                                           size_t ws_bytes, void* const* streams,
+                                           void* const* events);
+
 /* ------------------------------------------------------------- FP8 ----
  * FP8 (e4m3) dispatch and expert FFN: the MoE comm bottleneck page, section
  * 5.3, sends FP8 hidden states to halve the dispatch bytes; here the
@@ -340,6 +373,64 @@ MOE_API moe_status moe_layer_fwd_host_fp8(const moe_shape* s, int64_t n_micro,
                                   const uint8_t* W1q, const float* w1_scale, const uint8_t* W2q,
                                   const float* w2_scale, uint32_t* dev_status, void* ws,
                                   size_t ws_bytes, void* const* streams, void* const* events);
+
+/* ---------------------------------------------- expert parallelism ----
+ * Experts spread over `world` ranks, rank g holding the E/world consecutive
+ * experts g*E/world .. (g+1)*E/world - 1, and each token's rows sent to the
+ * rank of its expert and back: the dispatch and combine all-to-alls of the
+ * MoE comm bottleneck page, section 1.1 (byte counts in section 2.1), and
+ * the MoE module notes' MoELayer listing, section 4.2 (_all_to_all_routed).
+ * The library provides the per-rank steps; the exchanges themselves are the
+ * caller's collectives (e.g. NCCL all-to-all): rank r sends rows
+ * [offsets[g*E/world], offsets[(g+1)*E/world]) of its x_perm to rank g
+ * (send_counts[g] of them) and kept_counts[g*E/world ..] to rank g as its
+ * counts row r; rank g regroups what it received (moe_ep_regroup), runs
+ * moe_expert_ffn on its experts, regroups back and returns the rows in the
+ * same order; rank r then runs moe_combine on them as usual. */
+
+/* moe_permute for one rank of an expert-parallel group (s->T = this rank's
+ * tokens, s->E = all experts; world must divide E; 0 <= rank < world).
+ *   routed_all [world][E] int32 (device): every rank's routed counts (the
+ *        moe_route output, gathered from all ranks, this rank's row
+ *        included). Given, each expert serves the group's tokens in global
+ *        order - rank 0's tokens first, then rank 1's, ... - against the
+ *        capacity of the group's batch, C = max(1, ceil(cf * T_global*k / E)):
+ *        this rank keeps its assignment at local position pos iff the earlier
+ *        ranks' assignments to that expert plus pos are below C, which makes
+ *        the sharded layer equal to the single-device layer over all tokens.
+ *        NULL: the rank applies the capacity of its own batch (s->T) to its
+ *        own tokens alone, as the module notes' listing computes capacity
+ *        from the local batch; T_global is then ignored.
+ *   T_global: the group's tokens (>= s->T) when routed_all is given.
+ *   send_counts [world] int32 (device, out): rows for each rank's experts.
+ * Other arguments, results (expert-major x_perm, whose rows for rank g's
+ * experts are contiguous) and the workspace as moe_permute. */
+MOE_API moe_status moe_ep_permute(const moe_shape* s, int64_t world, int64_t rank,
+                                  const int32_t* routed_all, int64_t T_global,
+                                  const moe_bf16* x, const int32_t* topk_idx,
+                                  int32_t* kept_counts, int32_t* offsets, int32_t* dest_row,
+                                  int32_t* src_token, moe_bf16* x_perm, int32_t* send_counts,
+                                  uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* Moves rows of width H between the two orders of the rows a rank receives
+ * in an expert-parallel exchange:
+ *   source-major: from each source rank r in order, its rows of this rank's
+ *        E_local experts, expert by expert (what an all-to-all delivers);
+ *   expert-major: expert by expert, and within an expert source by source,
+ *        i.e. in global token order (what moe_expert_ffn takes).
+ *   counts [world][E_local] int32 (device): rows source r sent for local
+ *        expert e (row r is source r's kept_counts for these experts);
+ *        negative counts are read as 0.
+ *   to_expert_major 1: src source-major -> dst expert-major, and
+ *        local_offsets [E_local+1] (device, may be NULL) receives the
+ *        expert-major segment offsets for moe_expert_ffn; 0: the inverse
+ *        (src expert-major -> dst source-major; local_offsets unused).
+ *   rows: rows src and dst can hold; rows at or past it are not touched
+ *        (counts summing to more are cut there).
+ * world * E_local <= 256; H a multiple of 64. Needs no workspace. */
+MOE_API moe_status moe_ep_regroup(int64_t world, int64_t E_local, int64_t H, int64_t rows,
+                                  int to_expert_major, const int32_t* counts, const moe_bf16* src,
+                                  moe_bf16* dst, int32_t* local_offsets, void* stream);
 
 /* moe_permute for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it serves code that may not call

@@ -237,3 +237,26 @@ def test_binding_sizes_every_tensor_argument():
         assert moe._need(s, n) >= 1, n
     for n, v in want.items():
         assert moe._need(s, n) == v, n
+
+
+def test_expert_parallel_entries_reject_bad_arguments(lib):
+    s = _shape()                         # E experts in all
+    ws_need = _status(lib, s)[1]
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    args = lambda world, rank, routed_all, T_global, send: (
+        ctypes.byref(s), world, rank, routed_all, T_global, f, f, None, f, f, None, f, send, None,
+        f, ws_need, None)
+    E = s.E
+    assert lib.moe_ep_permute(*args(3 if E % 3 else 5, 0, None, 0, f)) == 2   # world must divide E
+    assert lib.moe_ep_permute(*args(2, 2, None, 0, f)) == 2                  # rank out of range
+    assert lib.moe_ep_permute(*args(2, -1, None, 0, f)) == 2
+    assert lib.moe_ep_permute(*args(2, 0, None, 0, None)) == 1              # send_counts required
+    assert lib.moe_ep_permute(*args(2, 0, f, s.T - 1, f)) == 2              # T_global < T
+    assert lib.moe_ep_permute(*args(2, 0, P(FAKE + 4), s.T, f)) == 5        # misaligned
+    # regroup: sizes and pointers
+    assert lib.moe_ep_regroup(0, 4, 64, 10, 1, f, f, f, None, None) == 2
+    assert lib.moe_ep_regroup(2, 200, 64, 10, 1, f, f, f, None, None) == 3  # > 256 experts
+    assert lib.moe_ep_regroup(2, 4, 96, 10, 1, f, f, f, None, None) == 3    # H % 64
+    assert lib.moe_ep_regroup(2, 4, 64, 10, 1, None, f, f, None, None) == 1
+    assert lib.moe_ep_regroup(2, 4, 64, 10, 1, f, None, f, None, None) == 1

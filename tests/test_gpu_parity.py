@@ -671,6 +671,40 @@ def test_layer_host_pipeline_equals_device_layer():
                               idx.cpu().numpy(), y_host[i], f"host pipeline micro-batch {i}")
 
 
+@pytest.mark.parametrize("T,H,E,k,h,n_micro", [(1000, 256, 12, 3, 320, 3), (2048, 256, 8, 2, 384, 4)])
+def test_layer_device_pipeline_equals_layer_and_oracle(T, H, E, k, h, n_micro):
+    """moe_layer_fwd_pipelined (dispatch and expert streams, alternate
+    workspaces): every micro-batch's y and aux are moe_layer_fwd's bits on
+    its rows, and its y matches the oracle. The second case runs the CTA-pair
+    GEMM (4096 rows per micro-batch)."""
+    w = W.custom(T, H, E, k, h, 1.0, "zipf", name="devpipe")
+    shape = _shape(T, H, E, k, h, 1.0)
+    base = W.make_inputs(w, seed=61)
+    xs = [W.make_inputs(w, seed=62 + i, with_weights=False)["x"] for i in range(n_micro)]
+    dv = {n: base[n].to(DEV) for n in ("gate", "W1", "W2", "bias")}
+    x_all = torch.cat(xs).to(DEV)
+    y_all = torch.full((n_micro * T, H), 7.0, dtype=torch.bfloat16, device=DEV)
+    aux_all = _zeros(n_micro, torch.float32)
+    status = _status()
+    pipe = moe.DevicePipeline(shape)
+    pipe.run(n_micro, x_all, dv["gate"], dv["bias"], dv["W1"], dv["W2"], y_all, aux_all,
+             status).synchronize()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ws = moe.Workspace(shape)
+    for i, x in enumerate(xs):
+        y = _zeros((T, H), torch.bfloat16)
+        aux = _zeros(1, torch.float32)
+        idx = _zeros((T, k), torch.int32)
+        moe.moe_layer_fwd(shape, x.to(DEV), dv["gate"], dv["bias"], dv["W1"], dv["W2"], y,
+                          aux=aux, topk_idx=idx, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y_all[i * T:(i + 1) * T].cpu(), y.cpu()), i
+        assert float(aux.item()) == float(aux_all[i].item())
+        _check_y_same_indices(x, base["gate"], base["bias"], base["W1"], base["W2"], k, 1.0,
+                              idx.cpu().numpy(), y.cpu(), f"device pipeline micro-batch {i}")
+
+
 # ============================================================ Gumbel router
 
 def _uniforms(T, E, seed):

@@ -25,6 +25,7 @@ __all__ = [
     "host_workspace_size", "HostPipeline", "moe_route_gumbel", "moe_layer_fwd_gumbel",
     "workspace_size_fp8", "moe_quantize_weights_fp8", "moe_layer_fwd_host_fp8", "moe_permute_fp8", "moe_expert_ffn_fp8",
     "moe_layer_fwd_fp8", "moe_combine_fp8", "Fp8Weights", "moe_expert_ffn_gathered",
+    "moe_ep_permute", "moe_ep_regroup", "DevicePipeline", "moe_layer_fwd_pipelined",
     "Workspace", "DEV_BAD_INDEX", "DEV_DUP_INDEX",
     "DEV_NONFINITE", "DEV_TIMEOUT", "LAYER_NUM_EVENTS", "EXPORTED_SYMBOLS", "build",
 ]
@@ -38,7 +39,8 @@ EXPORTED_SYMBOLS = ["moe_abi_version", "moe_capacity", "moe_workspace_size", "mo
                     "moe_layer_fwd_gumbel", "moe_workspace_size_fp8", "moe_quantize_weights_fp8",
                     "moe_permute_fp8", "moe_expert_ffn_fp8", "moe_layer_fwd_fp8",
                     "moe_combine_fp8", "moe_expert_ffn_gathered", "moe_host_workspace_size_fp8",
-                    "moe_layer_fwd_host_fp8"]
+                    "moe_layer_fwd_host_fp8", "moe_ep_permute", "moe_ep_regroup",
+                    "moe_pipelined_workspace_size", "moe_layer_fwd_pipelined"]
 
 
 class MoeError(RuntimeError):
@@ -118,6 +120,16 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_combine_fp8.argtypes = [S] + [_P] * 6
     lib.moe_layer_fwd_fp8.restype = ctypes.c_int
     lib.moe_layer_fwd_fp8.argtypes = [S] + [_P] * 18 + [ctypes.c_size_t, _P, _P]
+    lib.moe_pipelined_workspace_size.restype = ctypes.c_int
+    lib.moe_pipelined_workspace_size.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_layer_fwd_pipelined.restype = ctypes.c_int
+    lib.moe_layer_fwd_pipelined.argtypes = [S, ctypes.c_int64] + [_P] * 9 + [ctypes.c_size_t,
+                                                                           _P, _P]
+    I64 = ctypes.c_int64
+    lib.moe_ep_permute.restype = ctypes.c_int
+    lib.moe_ep_permute.argtypes = [S, I64, I64, _P, I64] + [_P] * 10 + [ctypes.c_size_t, _P]
+    lib.moe_ep_regroup.restype = ctypes.c_int
+    lib.moe_ep_regroup.argtypes = [I64, I64, I64, I64, ctypes.c_int] + [_P] * 5
     _lib = lib
     return lib
 
@@ -617,3 +629,96 @@ def moe_layer_fwd_fp8(shape, x, gate, gate_bias, q: Fp8Weights, y, aux=None, top
         a(P, torch.float32, "P"), a(kept_counts, torch.int32, "kept_counts"),
         a(offsets, torch.int32, "offsets"), a(dest_row, torch.int32, "dest_row"),
         a(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream), ev))
+
+
+# ------------------------------------------------- expert parallelism ----
+
+def moe_ep_permute(shape, world, rank, x, topk_idx, kept_counts, offsets, dest_row, src_token,
+                   x_perm, send_counts, routed_all=None, T_global=0, dev_status=None,
+                   ws: Workspace | None = None, stream=None):
+    """moe_permute for one rank of an expert-parallel group: with routed_all
+    ([world, E] int32, every rank's routed counts) experts serve the group's
+    tokens in global order against the group's capacity (T_global tokens);
+    without it the rank applies its own batch's capacity. send_counts
+    [world] receives the rows for each rank's experts."""
+    a = _Args(shape)
+    s = a.shape
+    wp, wn = _ws(ws, s)
+    ra = None
+    if routed_all is not None:
+        ra = _ptr(routed_all, torch.int32, "routed_all", int(world) * s.E)
+    _check("moe_ep_permute", load_library().moe_ep_permute(
+        ctypes.byref(s), int(world), int(rank), ra, int(T_global),
+        a(x, torch.bfloat16, "x"), a(topk_idx, torch.int32, "topk_idx"),
+        a(kept_counts, torch.int32, "kept_counts"), a(offsets, torch.int32, "offsets"),
+        a(dest_row, torch.int32, "dest_row"), a(src_token, torch.int32, "src_token"),
+        a(x_perm, torch.bfloat16, "x_perm"),
+        _ptr(send_counts, torch.int32, "send_counts", int(world)),
+        a(dev_status, torch.int32, "dev_status"), wp, wn, _stream(stream)))
+
+
+def moe_ep_regroup(world, E_local, counts, src, dst, to_expert_major, local_offsets=None,
+                   stream=None):
+    """Rows of src [rows, H] between the source-major order of an
+    expert-parallel exchange and the expert-major order of this rank's
+    experts (to_expert_major=True also fills local_offsets [E_local+1]);
+    counts [world, E_local] int32."""
+    rows, H = (src.shape[0], src.shape[1]) if src.dim() == 2 else (0, 0)
+    if dst.dim() != 2 or dst.shape[0] < rows or dst.shape[1] != H:
+        raise ValueError("dst must be [rows, H] like src")
+    _check("moe_ep_regroup", load_library().moe_ep_regroup(
+        int(world), int(E_local), int(H), int(rows), 1 if to_expert_major else 0,
+        _ptr(counts, torch.int32, "counts", int(world) * int(E_local)),
+        _ptr(src, torch.bfloat16, "src", rows * H) if rows else None,
+        _ptr(dst, torch.bfloat16, "dst", rows * H) if rows else None,
+        _ptr(local_offsets, torch.int32, "local_offsets", int(E_local) + 1),
+        _stream(stream)))
+
+
+# --------------------------------------------- on-device micro-batching ----
+
+class DevicePipeline:
+    """Owns what moe_layer_fwd_pipelined needs besides the weights: two
+    layer workspaces, a dispatch stream (high priority) and an expert stream,
+    and four events."""
+
+    def __init__(self, shape, device="cuda"):
+        self.shape = _shape(shape)
+        n = ctypes.c_size_t(0)
+        _check("moe_pipelined_workspace_size", load_library().moe_pipelined_workspace_size(
+            ctypes.byref(self.shape), ctypes.byref(n)))
+        self.nbytes = n.value
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        hi, _ = torch.cuda.Stream.priority_range()
+        self.streams = [torch.cuda.Stream(device=device, priority=hi),
+                        torch.cuda.Stream(device=device)]
+        self.events = [torch.cuda.Event() for _ in range(4)]
+        for e in self.events:          # create the handles
+            e.record(self.streams[0])
+
+    def run(self, n_micro, x, gate, gate_bias, W1, W2, y, aux=None, dev_status=None):
+        """Enqueues n_micro micro-batches (x, y: [n_micro*T, H] bf16 on the
+        device) after the work already queued on the current stream; returns
+        the dispatch stream, whose completion means y and aux are done."""
+        s = self.shape
+        cur = torch.cuda.current_stream()
+        for st in self.streams:
+            st.wait_stream(cur)
+        a = _Args(s)
+        n = int(n_micro) * s.T * s.H
+        st = (ctypes.c_void_p * 2)(*[q.cuda_stream for q in self.streams])
+        ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in self.events])
+        _check("moe_layer_fwd_pipelined", load_library().moe_layer_fwd_pipelined(
+            ctypes.byref(s), int(n_micro), _ptr(x, torch.bfloat16, "x", n),
+            a(gate, torch.bfloat16, "gate"), a(gate_bias, torch.float32, "gate_bias"),
+            a(W1, torch.bfloat16, "W1"), a(W2, torch.bfloat16, "W2"),
+            _ptr(y, torch.bfloat16, "y", n),
+            _ptr(aux, torch.float32, "aux", int(n_micro)),
+            a(dev_status, torch.int32, "dev_status"), self.buf.data_ptr(), self.nbytes, st, ev))
+        return self.streams[0]
+
+
+def moe_layer_fwd_pipelined(pipeline: DevicePipeline, n_micro, x, gate, gate_bias, W1, W2, y,
+                            aux=None, dev_status=None):
+    """C-ABI name for DevicePipeline.run."""
+    return pipeline.run(n_micro, x, gate, gate_bias, W1, W2, y, aux, dev_status)

@@ -19,7 +19,7 @@ LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
 OBJDIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["moe_api.cu", "moe_route.cu", "moe_dispatch.cu", "moe_gemm.cu", "moe_gemm_pair.cu", "moe_noalloc.cu",
-           "moe_fp8.cu"]
+           "moe_fp8.cu", "moe_ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

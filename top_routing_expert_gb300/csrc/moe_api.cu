@@ -67,6 +67,7 @@ struct Ws {
   float* aux;
   int32_t* kept;
   int32_t* offsets;
+  int32_t* cap;  // expert parallelism: this rank's capacity per expert
   uint32_t* status;
   uint32_t* ticket;
   int32_t* topk_idx;
@@ -126,6 +127,7 @@ size_t layout(const Dims& d, uint8_t* base, Ws* w, bool fp8 = false) {
   v.aux = static_cast<float*>(take(4));
   v.kept = static_cast<int32_t*>(take(static_cast<size_t>(d.E) * 4));
   v.offsets = static_cast<int32_t*>(take(static_cast<size_t>(d.E + 1) * 4));
+  v.cap = static_cast<int32_t*>(take(static_cast<size_t>(d.E) * 4));
   v.status = static_cast<uint32_t*>(take(4));
   v.ticket = static_cast<uint32_t*>(take(4));
   v.topk_idx = static_cast<int32_t*>(take(A * 4));
@@ -280,7 +282,8 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
   a.E_pad = d.E_pad;
   a.k = d.k;
   a.n_tiles = d.n_tiles;
-  a.stages = route_stages(d.E_pad);
+  a.gate_mode = kGateTransposed;
+  a.stages = 0;
   a.bias = bias;
   a.noise_u = noise.u;
   a.temperature = noise.temperature;
@@ -297,14 +300,20 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
   if (logits_in != nullptr) {
     MOE_CUDA(launch_route_logits(a, st));
   } else {
-    MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
-    CUtensorMap tm_x, tm_g, tm_rows;
+    CUtensorMap tm_x, tm_g;
     if (!tmap_bf16_2d(&tm_x, x, d.H, d.T, kBlockK, kTileTokens)) return MOE_ERR_CUDA;
-    if (!tmap_bf16_2d(&tm_g, w.gateT, d.H, d.E_pad, kBlockK, d.E_pad)) return MOE_ERR_CUDA;
-    // 256-column row pieces (512 B), used only for L2 prefetch
-    if (!tmap_bf16_2d(&tm_rows, x, d.H, d.T, 256, kTileTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return MOE_ERR_CUDA;
-    MOE_CUDA(launch_route_gemm(tm_x, tm_g, tm_rows, a, st, num_sms()));
+    // The gate [H,E] is the UMMA's B operand as given (MN-major TMA boxes of
+    // 64 experts) when E >= 64 and its rows are 16-byte multiples; otherwise
+    // a transposed, padded copy [E_pad,H] is made in the workspace first.
+    if (d.E >= 64 && d.E % 8 == 0 && tmap_bf16_2d(&tm_g, gate, d.E, d.H, 64, kBlockK)) {
+      a.gate_mode = kGateMnMajor;
+    } else {
+      a.gate_mode = kGateTransposed;
+      MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
+      if (!tmap_bf16_2d(&tm_g, w.gateT, d.H, d.E_pad, kBlockK, d.E_pad)) return MOE_ERR_CUDA;
+    }
+    a.stages = route_stages(d.E_pad, a.gate_mode);
+    MOE_CUDA(launch_route_gemm(tm_x, tm_g, a, st, num_sms()));
   }
   return MOE_OK;
 }
@@ -1059,6 +1068,191 @@ moe_status moe_layer_fwd_host(const moe_shape* s, int64_t n_micro, const moe_bf1
                               void* const* streams, void* const* events) {
   return layer_fwd_host(s, n_micro, x_host, y_host, aux_host, gate, gate_bias, W1, W2, nullptr,
                         dev_status, ws, ws_bytes, streams, events);
+}
+
+moe_status moe_pipelined_workspace_size(const moe_shape* s, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_NULL;
+  MOE_TRY(check_shape(s));
+  *bytes = 2 * layout(dims_of(s), nullptr, nullptr);
+  return MOE_OK;
+}
+
+// Micro-batch i uses layer workspace i % 2. Dispatch stream: route, scan and
+// permute of micro-batch i, then (once its GEMMs are done) the combine of
+// micro-batch i-1; expert stream: the two GEMMs of micro-batch i once its
+// permute is done. The permute of i+1 and the combine of i-1 thus run while
+// the GEMMs of i do, on the SM resources the GEMM leaves free. A workspace
+// is reused only after the combine that last read it, which precedes the
+// next route on the dispatch stream.
+moe_status moe_layer_fwd_pipelined(const moe_shape* s, int64_t n_micro, const moe_bf16* x,
+                                   const moe_bf16* gate, const float* gate_bias,
+                                   const moe_bf16* W1, const moe_bf16* W2, moe_bf16* y,
+                                   float* aux, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                                   void* const* streams, void* const* events) {
+  MOE_TRY(check_shape(s));
+  if (n_micro < 0 || s->T * n_micro >= (int64_t(1) << 31)) return MOE_ERR_SHAPE;
+  if (streams == nullptr || events == nullptr) return MOE_ERR_NULL;
+  for (int i = 0; i < 2; ++i)
+    if (streams[i] == nullptr) return MOE_ERR_NULL;
+  for (int i = 0; i < 4; ++i)
+    if (events[i] == nullptr) return MOE_ERR_NULL;
+  if (n_micro > 0) {
+    MOE_REQUIRE(x);
+    MOE_REQUIRE(y);
+  }
+  MOE_REQUIRE(gate);
+  MOE_REQUIRE(W1);
+  MOE_REQUIRE(W2);
+  MOE_OPTIONAL(gate_bias);
+  MOE_OPTIONAL(aux);
+  MOE_OPTIONAL(dev_status);
+  const Dims d = dims_of(s);
+  const size_t one = layout(d, nullptr, nullptr);
+  if (ws == nullptr) return MOE_ERR_NULL;
+  if (!aligned16(ws)) return MOE_ERR_ALIGN;
+  if (ws_bytes < 2 * one) return MOE_ERR_WORKSPACE;
+  Ws w[2];
+  layout(d, static_cast<uint8_t*>(ws), &w[0]);
+  layout(d, static_cast<uint8_t*>(ws) + one, &w[1]);
+  cudaStream_t sd = static_cast<cudaStream_t>(streams[0]);
+  cudaStream_t se = static_cast<cudaStream_t>(streams[1]);
+  cudaEvent_t ev_disp[2] = {static_cast<cudaEvent_t>(events[0]),
+                            static_cast<cudaEvent_t>(events[1])};
+  cudaEvent_t ev_ffn[2] = {static_cast<cudaEvent_t>(events[2]), static_cast<cudaEvent_t>(events[3])};
+  const size_t rows = static_cast<size_t>(d.T) * d.H;
+  auto combine_of = [&](int64_t i) -> moe_status {
+    const Ws& wb = w[i & 1];
+    MOE_CUDA(cudaStreamWaitEvent(sd, ev_ffn[i & 1], 0));
+    return run_combine(d, wb.y_perm, wb.dest_row, wb.topk_w, y + static_cast<size_t>(i) * rows, sd);
+  };
+  for (int64_t i = 0; i < n_micro; ++i) {
+    const Ws& wb = w[i & 1];
+    uint32_t* status = dev_status ? dev_status : wb.status;
+    const moe_bf16* xi = x + static_cast<size_t>(i) * rows;
+    if (d.T == 0) break;
+    RouteOut o{wb.topk_idx, wb.topk_w, wb.routed, wb.P, aux ? aux + i : nullptr, nullptr};
+    MOE_TRY(run_route(d, xi, gate, gate_bias, nullptr, o, status, wb, sd));
+    MOE_TRY(run_scan(d, true, wb.routed, wb.P, o.aux, wb.kept, wb.offsets, wb, sd));
+    MOE_TRY(run_gather(d, xi, wb.topk_idx, wb.offsets, wb.dest_row, wb.src_token, wb.x_perm,
+                       status, wb, sd));
+    MOE_CUDA(cudaEventRecord(ev_disp[i & 1], sd));
+    MOE_CUDA(cudaStreamWaitEvent(se, ev_disp[i & 1], 0));
+    MOE_TRY(run_gemm(d, wb.x_perm, W1, wb.offsets, d.H, d.h, wb.act, 1, status, se));
+    MOE_TRY(run_gemm(d, wb.act, W2, wb.offsets, d.h, d.H, wb.y_perm, 0, status, se));
+    MOE_CUDA(cudaEventRecord(ev_ffn[i & 1], se));
+    if (i >= 1) MOE_TRY(combine_of(i - 1));
+  }
+  if (n_micro > 0 && d.T > 0) MOE_TRY(combine_of(n_micro - 1));
+  if (d.T == 0 && aux != nullptr && n_micro > 0)
+    MOE_CUDA(cudaMemsetAsync(aux, 0, sizeof(float) * n_micro, sd));
+  return MOE_OK;
+}
+
+moe_status moe_ep_permute(const moe_shape* s, int64_t world, int64_t rank,
+                          const int32_t* routed_all, int64_t T_global, const moe_bf16* x,
+                          const int32_t* topk_idx, int32_t* kept_counts, int32_t* offsets,
+                          int32_t* dest_row, int32_t* src_token, moe_bf16* x_perm,
+                          int32_t* send_counts, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                          void* stream) {
+  MOE_TRY(check_shape(s));
+  if (world < 1 || rank < 0 || rank >= world || s->E % world != 0) return MOE_ERR_SHAPE;
+  MOE_REQUIRE(x);
+  MOE_REQUIRE(topk_idx);
+  MOE_REQUIRE(offsets);
+  MOE_REQUIRE(dest_row);
+  MOE_REQUIRE(x_perm);
+  MOE_REQUIRE(send_counts);
+  MOE_OPTIONAL(routed_all);
+  MOE_OPTIONAL(kept_counts);
+  MOE_OPTIONAL(src_token);
+  MOE_OPTIONAL(dev_status);
+  Dims d = dims_of(s);
+  if (routed_all != nullptr) {
+    // the capacity of the group's batch, served in global token order
+    if (T_global < s->T || T_global * s->top_k >= (int64_t(1) << 31)) return MOE_ERR_SHAPE;
+    d.C = moe_capacity(T_global, s->E, s->top_k, s->capacity_factor);
+  }
+  Ws w;
+  MOE_TRY(carve(s, d, ws, ws_bytes, &w));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = dev_status ? dev_status : w.status;
+  if (d.T == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d.E + 1), st));
+    MOE_CUDA(cudaMemsetAsync(send_counts, 0, sizeof(int32_t) * world, st));
+    if (kept_counts) MOE_CUDA(cudaMemsetAsync(kept_counts, 0, sizeof(int32_t) * d.E, st));
+    return MOE_OK;
+  }
+  RankArgs r;
+  r.T = d.T;
+  r.E = d.E;
+  r.k = d.k;
+  r.n_tiles = d.n_tiles;
+  r.topk_idx = topk_idx;
+  r.tile_cnt = w.tile_cnt;
+  r.rank8 = w.rank8;
+  r.ticket = w.ticket;
+  r.dev_status = status;
+  MOE_CUDA(launch_rank(r, st));
+  ScanArgs sc;
+  sc.T = d.T;
+  sc.E = d.E;
+  sc.k = d.k;
+  sc.n_tiles = d.n_tiles;
+  sc.C = d.C;
+  sc.tile_cnt = w.tile_cnt;
+  sc.tile_base = w.tile_base;
+  sc.ppart = nullptr;
+  sc.routed = w.routed;
+  sc.P = w.P;
+  sc.aux = nullptr;
+  sc.kept = kept_counts;
+  sc.offsets = offsets;
+  sc.ticket = w.ticket;
+  sc.routed_all = routed_all;
+  sc.world = static_cast<int>(world);
+  sc.rank = static_cast<int>(rank);
+  sc.cap = w.cap;
+  sc.send_counts = send_counts;
+  MOE_CUDA(launch_scan(sc, st));
+  GatherArgs g;
+  g.T = d.T;
+  g.H = d.H;
+  g.E = d.E;
+  g.k = d.k;
+  g.n_tiles = d.n_tiles;
+  g.C = d.C;
+  g.cap = routed_all != nullptr ? w.cap : nullptr;
+  g.x = x;
+  g.topk_idx = topk_idx;
+  g.rank8 = w.rank8;
+  g.tile_base = w.tile_base;
+  g.offsets = offsets;
+  g.dest_row = dest_row;
+  g.src_token = src_token;
+  g.x_perm = x_perm;
+  g.dev_status = status;
+  MOE_CUDA(launch_gather(g, num_sms(), st));
+  return MOE_OK;
+}
+
+moe_status moe_ep_regroup(int64_t world, int64_t E_local, int64_t H, int64_t rows,
+                          int to_expert_major, const int32_t* counts, const moe_bf16* src,
+                          moe_bf16* dst, int32_t* local_offsets, void* stream) {
+  if (world < 1 || E_local < 1 || H <= 0 || rows < 0) return MOE_ERR_SHAPE;
+  if (world * E_local > kMaxExperts || H % 64 != 0 || H > kMaxDim ||
+      rows >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_REQUIRE(counts);
+  MOE_OPTIONAL(local_offsets);
+  if (rows > 0) {
+    MOE_REQUIRE(src);
+    MOE_REQUIRE(dst);
+  }
+  MOE_CUDA(launch_ep_regroup(static_cast<int>(world), static_cast<int>(E_local),
+                             static_cast<int>(H), static_cast<int>(rows), to_expert_major ? 1 : 0,
+                             counts, src, dst, local_offsets, num_sms(),
+                             static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
 }
 
 moe_status moe_layer_fwd_host_fp8(const moe_shape* s, int64_t n_micro,

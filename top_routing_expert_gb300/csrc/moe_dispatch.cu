@@ -101,7 +101,16 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __threadfence();
 
   const int r = tid < a.E ? __ldcg(&a.routed[tid]) : 0;
-  const int kept = static_cast<int>(r < a.C ? r : a.C);
+  int64_t cap = a.C;
+  if (a.routed_all != nullptr && tid < a.E) {
+    // expert parallelism: the ranks before this one claim their assignments
+    // to the expert first (global token order), this rank gets what is left
+    int64_t before = 0;
+    for (int q = 0; q < a.rank; ++q) before += a.routed_all[static_cast<size_t>(q) * a.E + tid];
+    cap = a.C - before < 0 ? 0 : a.C - before;
+    if (a.cap) a.cap[tid] = static_cast<int32_t>(cap);
+  }
+  const int kept = static_cast<int>(r < cap ? r : cap);
   int all;
   const int off = block_exclusive_scan(tid < a.E ? kept : 0, shi, all);
   if (tid < a.E) {
@@ -109,6 +118,16 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     if (a.offsets) a.offsets[tid] = off;
   }
   if (tid == 0 && a.offsets) a.offsets[a.E] = all;
+  if (a.send_counts != nullptr) {
+    // rank g holds experts g*E/world .. (g+1)*E/world - 1: its rows are
+    // the offsets between those two expert boundaries
+    __shared__ int off_sh[kMaxExperts + 1];
+    if (tid < a.E) off_sh[tid] = off;
+    if (tid == 0) off_sh[a.E] = all;
+    __syncthreads();
+    const int per = a.E / a.world;
+    if (tid < a.world) a.send_counts[tid] = off_sh[(tid + 1) * per] - off_sh[tid * per];
+  }
   if (a.aux != nullptr) {
     double term = 0.0;
     if (tid < a.E && a.T > 0)
@@ -148,7 +167,8 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
       const int64_t row = static_cast<int64_t>(a.offsets[e]) + pos;
       // rows outside the buffer can only come from routing state left
       // incomplete by an aborted kernel (MOE_DEV_TIMEOUT): never written
-      if (pos >= 0 && pos < a.C && row >= 0 && row < rows) dest = static_cast<int>(row);
+      const int64_t cap = a.cap != nullptr ? a.cap[e] : a.C;
+      if (pos >= 0 && pos < cap && row >= 0 && row < rows) dest = static_cast<int>(row);
     }
     if (lane < a.k) {
       a.dest_row[static_cast<size_t>(t) * a.k + lane] = dest;

@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(GatherArgs a, uint8_t* 
       const int64_t pos = static_cast<int64_t>(a.tile_base[static_cast<size_t>(e) * a.n_tiles + t / kTileTokens]) +
                           a.rank8[static_cast<size_t>(t) * a.k + lane];
       const int64_t row = static_cast<int64_t>(a.offsets[e]) + pos;
-      if (pos >= 0 && pos < a.C && row >= 0 && row < rows) dest = static_cast<int>(row);
+      const int64_t cap = a.cap != nullptr ? a.cap[e] : a.C;
+      if (pos >= 0 && pos < cap && row >= 0 && row < rows) dest = static_cast<int>(row);
     }
     if (lane < a.k) {
       a.dest_row[static_cast<size_t>(t) * a.k + lane] = dest;

@@ -20,6 +20,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;      // waits for in-flight cop
 // Router epilogue arguments (GEMM and logits entry points).
 struct RouteArgs {
   int T, H, E, E_pad, k, n_tiles, stages;
+  int gate_mode;           // how the gate reaches shared memory (kGate* below)
   const float* bias;       // [E] or nullptr (GEMM path only)
   const float* noise_u;    // [T,E] uniforms in [0,1) for Gumbel noise, or nullptr
   float temperature;       // scores = (logits + gumbel(u)) / temperature when noise_u
@@ -57,11 +58,19 @@ struct ScanArgs {
   int32_t* kept;            // [E] or nullptr
   int32_t* offsets;         // [E+1] or nullptr
   uint32_t* ticket;
+  // expert parallelism (all nullptr / 0 otherwise): the experts are spread
+  // over `world` ranks (E/world consecutive experts each) and every expert
+  // serves the group's tokens in global order, rank after rank
+  const int32_t* routed_all = nullptr;  // [world][E] assignments of every rank, before drops
+  int world = 1, rank = 0;
+  int32_t* cap = nullptr;               // [E] out: this rank's capacity left per expert
+  int32_t* send_counts = nullptr;       // [world] out: kept rows for each rank's experts
 };
 
 struct GatherArgs {
   int T, H, E, k, n_tiles;
   int64_t C;
+  const int32_t* cap = nullptr;  // [E] per-expert capacity (expert parallelism), else C
   const uint16_t* x;
   const int32_t* topk_idx;
   const uint8_t* rank8;
@@ -107,15 +116,33 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-int route_stages(int E_pad);
-size_t route_smem_bytes(int E_pad, int stages);
+// How the router's B operand (the gate, N = E_pad experts x K = H) reaches
+// each pipeline stage:
+//   kGateTransposed - TMA from a transposed, zero-padded copy [E_pad, H] made
+//                     in the workspace by a separate kernel (K-major rows:
+//                     E_pad TMA rows of 128 bytes per stage);
+//   kGateMnMajor    - TMA from the gate [H, E] as given, MN-major, in boxes of
+//                     64 experts x 64 k (E % 8 == 0, so rows are 16-byte
+//                     multiples). Used for E >= 64, where the boxes are full;
+//                     for fewer experts most of each box is zero fill, and 64
+//                     TMA rows per stage instead of E_pad slow the router
+//                     (large-expert router 76 -> 93 us on GB300).
+enum { kGateTransposed = 0, kGateMnMajor = 1 };
+
+// Shared-memory bytes of the gate per 64-deep k-block stage.
+__host__ __device__ inline uint32_t route_gate_stage_bytes(int E_pad, int gate_mode) {
+  return gate_mode == kGateMnMajor ? static_cast<uint32_t>((E_pad + 63) / 64) * 8192u
+                                   : static_cast<uint32_t>(E_pad) * kBlockK * 2;
+}
+
 size_t gemm_smem_bytes(int E);
 
 cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, int E, int E_pad,
                                   cudaStream_t st);
+int route_stages(int E_pad, int gate_mode);
+size_t route_smem_bytes(int E_pad, int stages, int gate_mode);
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st,
-                              int num_sms);
+                              const RouteArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st);
 cudaError_t launch_rank(const RankArgs& a, cudaStream_t st);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st);
@@ -138,5 +165,10 @@ cudaError_t launch_row_quant(const uint16_t* src, const uint32_t* amax, uint8_t*
                              int num_sms, cudaStream_t st);
 cudaError_t launch_gather_fp8(const GatherArgs& a, uint8_t* xq, float* xs, int num_sms,
                               cudaStream_t st);
+// Rows between the source-major order a rank receives them in and the
+// expert-major order of its experts (expert parallelism).
+cudaError_t launch_ep_regroup(int world, int E_loc, int H, int rows, int to_expert_major,
+                              const int32_t* counts, const uint16_t* src, uint16_t* dst,
+                              int32_t* local_offsets, int num_sms, cudaStream_t st);
 
 }  // namespace moe

@@ -16,8 +16,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kRowGroup = 4;           // k-blocks per 512-byte row prefetch
-constexpr int kRouteGroupsAhead = 2;   // row prefetches in flight ahead of the loads
 
 // ----------------------------------------------------------- top-k list ----
 
@@ -378,6 +376,34 @@ __global__ void gate_transpose_kernel(const uint16_t* __restrict__ gate,
   }
 }
 
+// The gate's part of one pipeline stage (k rows kb*64 .. kb*64+63): one box
+// of the transposed gate [E_pad, H], or ceil(E_pad/64) boxes of 64 expert
+// columns of the gate [H, E] as given (inner coordinate a multiple of 64
+// elements, so every box starts on a 128-byte boundary).
+__device__ __forceinline__ void load_gate_stage(uint8_t* dst, const CUtensorMap* tm_gate,
+                                                uint64_t* bar, int kb, const RouteArgs& a) {
+  if (a.gate_mode == kGateMnMajor) {
+    for (int cb = 0; cb < (a.E_pad + 63) / 64; ++cb)
+      tma_load_2d(dst + 8192 * cb, tm_gate, bar, 64 * cb, kb * kBlockK);
+  } else {
+    tma_load_2d(dst, tm_gate, bar, kb * kBlockK, 0);
+  }
+}
+
+// UMMA descriptors of the gate (the B operand, N = E_pad) for the kk-th
+// 16-deep K step of a stage: K-major 128-byte rows (32 bytes per step), or
+// MN-major 128-byte rows of 64 experts, one per k (16 rows = 2 KB per step,
+// 64-column blocks 8 KB apart).
+__device__ __forceinline__ uint64_t route_gate_desc(uint32_t b_addr, int kk, int gate_mode) {
+  return gate_mode == kGateMnMajor ? smem_desc_sw128(b_addr + 2048u * kk, 8192u, 1024u)
+                                   : smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
+}
+
+__device__ __forceinline__ uint32_t route_idesc(const RouteArgs& a) {
+  return idesc_bf16_f32(kTileTokens, static_cast<uint32_t>(a.E_pad), false,
+                        a.gate_mode == kGateMnMajor);
+}
+
 // Shared-memory carve-up of the router kernel after the 1024-aligned
 // pipeline stages (the stages are reused as epilogue scratch once the
 // accumulator is complete).
@@ -412,8 +438,7 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
 template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens * 8, 1)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
-                      const __grid_constant__ CUtensorMap tm_gate,
-                      const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
+                      const __grid_constant__ CUtensorMap tm_gate, RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   const int ecols = npart * cpt;                // columns the epilogue reads (>= E)
   const int E32 = ((ecols > a.E_pad ? ecols : a.E_pad) + 31) & ~31;
   const uint32_t a_bytes = kTileTokens * kBlockK * 2;
-  const uint32_t b_bytes = static_cast<uint32_t>(a.E_pad) * kBlockK * 2;
+  const uint32_t b_bytes = route_gate_stage_bytes(a.E_pad, a.gate_mode);
   const uint32_t stage_bytes = a_bytes + b_bytes;
   RouteSmem sm = carve_route_smem(smem + static_cast<size_t>(S) * stage_bytes, S, E32);
   const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(E32));
@@ -457,12 +482,9 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   const int nk = a.H / kBlockK;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer. The swizzled loads read 128-byte pieces of rows that lie
-    // H*2 bytes apart; ahead of them, L2 prefetches through a plain (no
-    // swizzle) map fetch 512 contiguous bytes of each of the tile's rows.
-    const int n_groups = (nk + kRowGroup - 1) / kRowGroup;
-    for (int g = 0; g < kRouteGroupsAhead && g < n_groups; ++g)
-      tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
+    // TMA producer: the tile's 128 rows x 64 k of x and the gate's k-block
+    // per stage (an L2 prefetch of whole 512-byte row pieces ahead of these
+    // loads measured 2-8 % slower and was dropped)
     int kb = 0;
     for (; kb < nk; ++kb) {
       const int s = kb % S;
@@ -470,12 +492,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
       uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
       mbar_arrive_expect_tx(&sm.full[s], stage_bytes);
       tma_load_2d(st, &tm_x, &sm.full[s], kb * kBlockK, tile * kTileTokens);
-      tma_load_2d(st + a_bytes, &tm_gate, &sm.full[s], kb * kBlockK, 0);
-      if (kb % kRowGroup == 0) {
-        const int g = kb / kRowGroup + kRouteGroupsAhead;
-        if (g < n_groups)
-          tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
-      }
+      load_gate_stage(st + a_bytes, &tm_gate, &sm.full[s], kb, a);
     }
     if (kb < nk) {
       // aborted: let the loads already issued land before the CTA exits
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // UMMA issuer: D[128 x E_pad] += X[128 x 64] * gate^T[64 x E_pad] per stage
-    const uint32_t idesc = idesc_bf16_f32(kTileTokens, static_cast<uint32_t>(a.E_pad), false, false);
+    const uint32_t idesc = route_idesc(a);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S;
       if (!mbar_wait(&sm.full[s], (kb / S) & 1, wc)) break;
@@ -494,8 +511,8 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
 #pragma unroll
       for (int kk = 0; kk < kBlockK / 16; ++kk) {
         const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-        const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
-        umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        umma_bf16(tmem, ad, route_gate_desc(b_addr, kk, a.gate_mode), idesc,
+                  (kb | kk) != 0 ? 1u : 0u);
       }
       umma_commit(&sm.empty[s]);
     }
@@ -549,13 +566,13 @@ struct PersistLayout {
   size_t off_bar, off_bias, off_masks, off_red, off_epi, total;
 };
 
-__host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int kmax) {
+__host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int kmax, int gate_mode) {
   PersistLayout L;
   L.npart = persist_parts_of(E);
   L.cpt = persist_cpt_of(E);
   const int ecols = L.npart * L.cpt;
   L.E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
-  L.stage_bytes = static_cast<uint32_t>(kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2);
+  L.stage_bytes = static_cast<uint32_t>(kTileTokens * kBlockK * 2) + route_gate_stage_bytes(E_pad, gate_mode);
   int c = 32;
   while (c < 2 * L.E32) c <<= 1;
   L.ncols = static_cast<uint32_t>(c);
@@ -574,12 +591,11 @@ __host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int km
 template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
     route_persistent_kernel(const __grid_constant__ CUtensorMap tm_x,
-                            const __grid_constant__ CUtensorMap tm_gate,
-                            const __grid_constant__ CUtensorMap tm_x_rows, RouteArgs a) {
+                            const __grid_constant__ CUtensorMap tm_gate, RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX);
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode);
   const int S = L.S, E32 = L.E32;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   uint64_t* empty = full + S;
@@ -634,10 +650,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool aborted = false;
-      const int n_groups = (nk + kRowGroup - 1) / kRowGroup;
       for (int tile = blockIdx.x; tile < a.n_tiles && !aborted; tile += gridDim.x) {
-        for (int g = 0; g < kRouteGroupsAhead && g < n_groups; ++g)
-          tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             aborted = true;
@@ -646,12 +659,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
           uint8_t* st = smem + static_cast<size_t>(stage) * L.stage_bytes;
           mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
           tma_load_2d(st, &tm_x, &full[stage], kb * kBlockK, tile * kTileTokens);
-          tma_load_2d(st + a_bytes, &tm_gate, &full[stage], kb * kBlockK, 0);
-          if (kb % kRowGroup == 0) {
-            const int g = kb / kRowGroup + kRouteGroupsAhead;
-            if (g < n_groups)
-              tma_prefetch_l2_2d(&tm_x_rows, g * kRowGroup * kBlockK, tile * kTileTokens);
-          }
+          load_gate_stage(st + a_bytes, &tm_gate, &full[stage], kb, a);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -674,8 +682,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------- UMMA issuer ----
-      const uint32_t idesc =
-          idesc_bf16_f32(kTileTokens, static_cast<uint32_t>(a.E_pad), false, false);
+      const uint32_t idesc = route_idesc(a);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -696,8 +703,8 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, ad, route_gate_desc(b_addr, kk, a.gate_mode), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == S) {
@@ -811,18 +818,19 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 
 // ------------------------------------------------------------------ host ----
 
-int route_stages(int E_pad) {
-  // as many stages as fit in ~108 KB (two CTAs' worth per SM)
-  const int stage = kTileTokens * kBlockK * 2 + E_pad * kBlockK * 2;
-  int s = (108 * 1024) / stage;
-  return s < 2 ? 2 : (s > 6 ? 6 : s);
+int route_stages(int E_pad, int gate_mode) {
+  // the per-tile kernel runs with at most one CTA per SM (no more tiles
+  // than SMs): as many stages as fit in ~200 KB
+  const int stage = kTileTokens * kBlockK * 2 + static_cast<int>(route_gate_stage_bytes(E_pad, gate_mode));
+  int s = (200 * 1024) / stage;
+  return s < 2 ? 2 : (s > 10 ? 10 : s);
 }
 
-size_t route_smem_bytes(int E_pad, int stages) {
+size_t route_smem_bytes(int E_pad, int stages, int gate_mode) {
   const int E = E_pad;  // upper bound for the epilogue's column span
   const int ecols = route_parts_of(E) * route_cpt_of(E);
   const int E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
-  const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(E_pad) * kBlockK * 2;
+  const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + route_gate_stage_bytes(E_pad, gate_mode);
   return 1024 + stage * stages + 8 * (2 * stages + 1) + 16 + 4 * E32 + 2 * 4 * 4 * E32;
 }
 
@@ -837,26 +845,25 @@ cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, 
 
 template <int KMAX>
 cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                                const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st) {
+                                const RouteArgs& a, cudaStream_t st) {
   const int npart = route_parts_of(a.E);
   // the epilogue scratch lives in the pipeline stages once they are free
   const size_t stage_area = static_cast<size_t>(a.stages) *
-                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + static_cast<size_t>(a.E_pad) * kBlockK * 2);
+                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + route_gate_stage_bytes(a.E_pad, a.gate_mode));
   if (epi_scratch_bytes(npart, KMAX) > stage_area) return cudaErrorInvalidConfiguration;
-  const size_t smem = route_smem_bytes(a.E_pad, a.stages);
+  const size_t smem = route_smem_bytes(a.E_pad, a.stages, a.gate_mode);
   cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(tm_x, tm_gate, tm_x_rows, a);
+  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(tm_x, tm_gate, a);
   return cudaGetLastError();
 }
 
 template <int KMAX>
 cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                                      const CUtensorMap& tm_x_rows, const RouteArgs& a,
-                                      int num_sms, cudaStream_t st) {
-  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX);
+                                      const RouteArgs& a, int num_sms, cudaStream_t st) {
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode);
   if (L.S < 2) return cudaErrorInvalidConfiguration;
   cudaError_t err = cudaFuncSetAttribute(route_persistent_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -864,7 +871,7 @@ cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap
   if (err != cudaSuccess) return err;
   const int grid = a.n_tiles < num_sms ? a.n_tiles : num_sms;
   route_persistent_kernel<KMAX><<<grid, kTileTokens + kTileTokens * L.npart, L.total, st>>>(
-      tm_x, tm_gate, tm_x_rows, a);
+      tm_x, tm_gate, a);
   return cudaGetLastError();
 }
 
@@ -873,18 +880,17 @@ bool route_use_persistent(const RouteArgs& a, int num_sms) {
 }
 
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
-                              const CUtensorMap& tm_x_rows, const RouteArgs& a, cudaStream_t st,
-                              int num_sms) {
+                              const RouteArgs& a, cudaStream_t st, int num_sms) {
   if (route_use_persistent(a, num_sms)) {
-    if (a.k <= 2) return launch_route_persistent_k<2>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
-    if (a.k <= 4) return launch_route_persistent_k<4>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
-    if (a.k <= 6) return launch_route_persistent_k<6>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
-    return launch_route_persistent_k<8>(tm_x, tm_gate, tm_x_rows, a, num_sms, st);
+    if (a.k <= 2) return launch_route_persistent_k<2>(tm_x, tm_gate, a, num_sms, st);
+    if (a.k <= 4) return launch_route_persistent_k<4>(tm_x, tm_gate, a, num_sms, st);
+    if (a.k <= 6) return launch_route_persistent_k<6>(tm_x, tm_gate, a, num_sms, st);
+    return launch_route_persistent_k<8>(tm_x, tm_gate, a, num_sms, st);
   }
-  if (a.k <= 2) return launch_route_gemm_k<2>(tm_x, tm_gate, tm_x_rows, a, st);
-  if (a.k <= 4) return launch_route_gemm_k<4>(tm_x, tm_gate, tm_x_rows, a, st);
-  if (a.k <= 6) return launch_route_gemm_k<6>(tm_x, tm_gate, tm_x_rows, a, st);
-  return launch_route_gemm_k<8>(tm_x, tm_gate, tm_x_rows, a, st);
+  if (a.k <= 2) return launch_route_gemm_k<2>(tm_x, tm_gate, a, st);
+  if (a.k <= 4) return launch_route_gemm_k<4>(tm_x, tm_gate, a, st);
+  if (a.k <= 6) return launch_route_gemm_k<6>(tm_x, tm_gate, a, st);
+  return launch_route_gemm_k<8>(tm_x, tm_gate, a, st);
 }
 
 template <int KMAX>
