@@ -60,12 +60,15 @@ def test_gpu_arm_report_has_the_contract_keys():
     stage = [0.075, 0.014, 0.12, 4.8, 4.6, 0.11]
     clk = {"sm_mhz": 1780.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 5}
     e2e = {"ms": 10.0, "h2d": w.T * w.H * 2, "d2h": w.T * w.H * 2 + 4}
-    line = bench.report(args, w, 1, sum(stage), stage, clk, 0, 65536, 32768, e2e, None,
-                        "inputs larger than L2", dense=4.6)
+    m = {"ms": sum(stage), "stage_ms": stage, "status": 0, "n_kept": 65536, "any_kept": 32768,
+         "l2": "inputs larger than L2", "steps": 100, "host_window": (0.0, 1.0)}
+    line = bench.report(args, w, 1, m, clk, e2e, None, dense=4.6)
     _check_base(line)
     rf = line["roofline"]
     assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s"
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+    # the timed region is well under a second: the burst peak is the roofline
+    assert rf["peak"] == bench.peaks()["bf16_tflops"]
     # achieved = the GEMMs' algorithmic FLOP over their event time
     flop = 4 * 65536 * w.H * w.h
     assert abs(rf["achieved"] - flop / (9.4e-3) / 1e12) < 1.0
@@ -74,6 +77,23 @@ def test_gpu_arm_report_has_the_contract_keys():
     assert line["clocks"]["reasons"] == ["sw_power_cap"]
     assert line["moe_vs_dense_ffn"]["ratio"] == round(sum(stage) / 4.6, 3)
     json.dumps(line)  # serialisable
+    # a per-workload entry has the same accounting, FP8 against twice the peak
+    kr = bench.kernel_report(w, m, True)
+    assert kr["roofline"]["peak"] == 2 * bench.peaks()["bf16_tflops"]
+    assert kr["value"] == round(w.T / (sum(stage) / 1e3), 1)
+
+
+def test_clock_window_keeps_samples_of_the_timed_region_only(tmp_path):
+    import bench
+    c = bench.ClockSampler(0)
+    row = lambda t, mhz, cap: [t, "0", str(mhz), "2070", "900.0", "0x0", "Not Active",
+                               "Not Active", "Not Active", cap]
+    c.rows = [row(0.9, 2070, "Not Active"), row(1.01, 1500, "Active"),
+              row(1.06, 1600, "Active"), row(1.11, 1700, "Not Active"),
+              row(1.5, 2070, "Not Active")]
+    win = c.window(1.0, 1.1)
+    assert win["samples"] == 3 and win["sm_mhz"] == 1600
+    assert win["reasons"] == ["sw_power_cap"] and win["sm_max_mhz"] == 2070
 
 
 def test_reference_arm_under_torchrun_prints_once():

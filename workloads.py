@@ -139,6 +139,34 @@ def make_inputs(w: Workload, seed: int = 0, with_weights: bool = True) -> dict:
     return out
 
 
+def make_inputs_on_device(w: Workload, device, seed: int = 0) -> dict:
+    """The same distributions as ``make_inputs`` (and the same bias rule),
+    drawn by a seeded generator on ``device``: a different but equally
+    seeded stream of numbers, for timing runs of the larger workloads where
+    drawing gigabytes of weights on the host would take half a minute. The
+    parity tests use ``make_inputs``."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=gen, dtype=torch.float32, device=device) * std
+                ).to(torch.bfloat16)
+
+    x = draw((w.T, w.H), 1.0)
+    gate = draw((w.H, w.E), 1.0 / math.sqrt(w.H))
+    if w.bias == "normal1.5":
+        bias = torch.randn((w.E,), generator=gen, dtype=torch.float32, device=device) * \
+            math.sqrt(1.5)
+    else:
+        b = bias_vector(w)
+        bias = None if b is None else b.to(device)
+    W1 = torch.empty((w.E, w.H, w.h), dtype=torch.bfloat16, device=device)
+    W2 = torch.empty((w.E, w.h, w.H), dtype=torch.bfloat16, device=device)
+    for e in range(w.E):
+        W1[e] = draw((w.H, w.h), 1.0 / math.sqrt(w.H))
+        W2[e] = draw((w.h, w.H), 1.0 / math.sqrt(w.h))
+    return {"x": x, "gate": gate, "bias": bias, "W1": W1, "W2": W2}
+
+
 def make_logits(T: int, E: int, seed: int = 0, bias: Optional[torch.Tensor] = None,
                 quantum: float = 0.0) -> torch.Tensor:
     """Synthetic fp32 router logits [T,E] ~ N(0,1) (+ bias), for the
