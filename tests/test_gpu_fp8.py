@@ -489,6 +489,16 @@ def test_layer_fp8_captured_in_a_cuda_graph():
         x_static.copy_(x)
         g.replay()
         y = _zeros((w.T, w.H), torch.bfloat16)
-        moe.moe_layer_fwd_fp8(s, x, gate, bias, Q, y, ws=ws_direct)
+        idx = _zeros((w.T, w.k), torch.int32)
+        moe.moe_layer_fwd_fp8(s, x, gate, bias, Q, y, topk_idx=idx, ws=ws_direct)
         torch.cuda.synchronize()
         assert torch.equal(y_static, y), seed
+        # the replayed outputs against the oracle's FP8 layer on the GPU's indices
+        gidx = idx.cpu().numpy()
+        lg = oracle_logits_chunked(x.cpu(), base["gate"], base["bias"])
+        r = O.route_from_logits(lg, w.k)
+        routing_flips(gidx, r.idx, topk_margins(lg, w.k), f"fp8 graph replay {seed}")
+        d = O.dispatch_plan(gidx, w.E, O.capacity(w.T, w.E, w.k, w.cf))
+        ref = O.token_outputs_fp8(np64(x.cpu()), gidx, O.renormalise(r.p, gidx), d.dest_row >= 0,
+                                  _LazyQ(base["W1"]), _LazyQ(base["W2"]), fp8_combine=True)
+        assert_fp8_out_close(np64(y_static.cpu()), ref, f"fp8 graph replay {seed}")

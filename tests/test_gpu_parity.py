@@ -327,6 +327,9 @@ def _ffn_gpu(s, xp, off, W1, W2):
     # >= 4096 rows: the CTA-pair kernel, with empty, 1-row and odd-m-tile segments
     (6, 128, 192, [0, 1, 129, 4000, 257, 1]),
     (3, 256, 320, [2048, 0, 2176]),
+    # 16 experts on the pair path, with odd m-tile counts whose last m-tile
+    # is full, partial or one row
+    (16, 256, 320, [0, 1, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 640, 700, 900]),
 ])
 def test_expert_ffn_against_oracle(E, H, h, counts):
     T, N, xp, W1, W2, off = _ffn_case(E, H, h, counts, seed=E + H)
@@ -852,8 +855,12 @@ def test_layer_captured_in_a_cuda_graph():
         g.replay()
         y = _zeros((w.T, w.H), torch.bfloat16)
         aux = _zeros(1, torch.float32)
+        idx = _zeros((w.T, w.k), torch.int32)
         moe.moe_layer_fwd(s, x, dv["gate"], dv["bias"], dv["W1"], dv["W2"], y, aux=aux,
-                          ws=ws_direct)
+                          topk_idx=idx, ws=ws_direct)
         torch.cuda.synchronize()
         assert torch.equal(y_static, y), seed
         assert torch.equal(aux_static, aux), seed
+        # and the replayed outputs against the oracle
+        _check_y_same_indices(x.cpu(), base["gate"], base["bias"], base["W1"], base["W2"], w.k,
+                              w.cf, idx.cpu().numpy(), y_static.cpu(), f"graph replay {seed}")

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int shi[kScanThreads / 32 + 1];
   __shared__ double shd[kScanThreads];
   __shared__ int last;
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int e = blockIdx.x, tid = threadIdx.x;
   const int n = a.n_tiles;
   const int per = (n + kScanThreads - 1) / kScanThreads;
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
 // One warp per token. Lane j < k owns slot j.
 template <int U>
 __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 3;  // 16-byte vectors per row
@@ -214,6 +218,8 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 // in flight together.
 template <int KMAX, int U>
 __global__ void __launch_bounds__(256, (KMAX * U > 8) ? 2 : 3) combine_kernel(CombineArgs a) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 3;
@@ -290,29 +296,22 @@ int warp_grid(int T, int num_sms) {
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t st) {
-  scan_kernel<<<a.E, kScanThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(scan_kernel, dim3(a.E), dim3(kScanThreads), 0, st, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, int num_sms, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   const int grid = warp_grid(a.T, num_sms);
-  gather_kernel<8><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel<8>, dim3(grid), dim3(256), 0, st, a);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   const int grid = warp_grid(a.T, num_sms);
-  if (a.k <= 2)
-    combine_kernel<2, 4><<<grid, 256, 0, st>>>(a);
-  else if (a.k <= 4)
-    combine_kernel<4, 2><<<grid, 256, 0, st>>>(a);
-  else if (a.k <= 6)
-    combine_kernel<6, 2><<<grid, 256, 0, st>>>(a);
-  else
-    combine_kernel<8, 1><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.k <= 2) return launch_pdl(combine_kernel<2, 4>, dim3(grid), dim3(256), 0, st, a);
+  if (a.k <= 4) return launch_pdl(combine_kernel<4, 2>, dim3(grid), dim3(256), 0, st, a);
+  if (a.k <= 6) return launch_pdl(combine_kernel<6, 2>, dim3(grid), dim3(256), 0, st, a);
+  return launch_pdl(combine_kernel<8, 1>, dim3(grid), dim3(256), 0, st, a);
 }
 
 }  // namespace moe

@@ -13,6 +13,7 @@
 // With sources in rank order inside an expert, the expert-major rows of an
 // expert are its rows in global token order, rank after rank.
 #include "moe_internal.h"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kRegroupThreads)
   __shared__ int scan_sh[kRegroupThreads];
   __shared__ int src_off[kRegroupThreads + 1];  // rows before block b, source-major
   __shared__ int exp_off[kRegroupThreads + 1];  // rows before block j, expert-major
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int n = world * E_loc;
   const int tid = threadIdx.x;
   // source-major block b = r * E_loc + e; expert-major block j = e * world + r
@@ -99,10 +102,9 @@ cudaError_t launch_ep_regroup(int world, int E_loc, int H, int rows, int to_expe
   const int cap = num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  regroup_kernel<<<blocks, kRegroupThreads, 0, st>>>(
-      world, E_loc, H, rows, to_expert_major, counts, reinterpret_cast<const uint4*>(src),
-      reinterpret_cast<uint4*>(dst), local_offsets);
-  return cudaGetLastError();
+  return launch_pdl(regroup_kernel, dim3(blocks), dim3(kRegroupThreads), 0, st, world, E_loc, H,
+                    rows, to_expert_major, counts, reinterpret_cast<const uint4*>(src),
+                    reinterpret_cast<uint4*>(dst), local_offsets);
 }
 
 }  // namespace moe

@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(256) row_quant_kernel(const uint16_t* __restri
                                                         float* __restrict__ scale,
                                                         const int32_t* __restrict__ offsets,
                                                         int E, int rows, int K) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   int n = offsets[E];
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(256) row_quant_kernel(const uint16_t* __restri
 // destination, with the scale. Destinations as in the bf16 gather.
 __global__ void __launch_bounds__(256) gather_fp8_kernel(GatherArgs a, uint8_t* __restrict__ xq,
                                                          float* __restrict__ xs) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 3;
@@ -261,6 +265,8 @@ template <int KMAX, int U>
 __global__ void __launch_bounds__(256, 2) combine_fp8_kernel(CombineArgs a,
                                                              const uint8_t* __restrict__ y_q,
                                                              const float* __restrict__ y_scale) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = a.H >> 4;
@@ -342,15 +348,10 @@ cudaError_t launch_combine_fp8(const CombineArgs& a, const uint8_t* y_q, const f
   if (a.T == 0) return cudaSuccess;
   int grid = (a.T + 7) / 8;
   if (grid > num_sms * 8) grid = num_sms * 8;
-  if (a.k <= 2)
-    combine_fp8_kernel<2, 3><<<grid, 256, 0, st>>>(a, y_q, y_scale);
-  else if (a.k <= 4)
-    combine_fp8_kernel<4, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
-  else if (a.k <= 6)
-    combine_fp8_kernel<6, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
-  else
-    combine_fp8_kernel<8, 1><<<grid, 256, 0, st>>>(a, y_q, y_scale);
-  return cudaGetLastError();
+  if (a.k <= 2) return launch_pdl(combine_fp8_kernel<2, 3>, dim3(grid), dim3(256), 0, st, a, y_q, y_scale);
+  if (a.k <= 4) return launch_pdl(combine_fp8_kernel<4, 1>, dim3(grid), dim3(256), 0, st, a, y_q, y_scale);
+  if (a.k <= 6) return launch_pdl(combine_fp8_kernel<6, 1>, dim3(grid), dim3(256), 0, st, a, y_q, y_scale);
+  return launch_pdl(combine_fp8_kernel<8, 1>, dim3(grid), dim3(256), 0, st, a, y_q, y_scale);
 }
 
 cudaError_t launch_quantize_weights(const uint16_t* W, uint8_t* Wq, float* Ws, int E, int K,
@@ -376,8 +377,8 @@ cudaError_t launch_row_quant(const uint16_t* src, const uint32_t* amax, uint8_t*
   if (rows == 0) return cudaSuccess;
   int grid = (rows + 7) / 8;
   if (grid > num_sms * 8) grid = num_sms * 8;
-  row_quant_kernel<<<grid, 256, 0, st>>>(src, amax, dst, scale, offsets, E, rows, K);
-  return cudaGetLastError();
+  return launch_pdl(row_quant_kernel, dim3(grid), dim3(256), 0, st, src, amax, dst, scale, offsets,
+                    E, rows, K);
 }
 
 cudaError_t launch_gather_fp8(const GatherArgs& a, uint8_t* xq, float* xs, int num_sms,
@@ -385,8 +386,7 @@ cudaError_t launch_gather_fp8(const GatherArgs& a, uint8_t* xq, float* xs, int n
   if (a.T == 0) return cudaSuccess;
   int grid = (a.T + 7) / 8;
   if (grid > num_sms * 8) grid = num_sms * 8;
-  gather_fp8_kernel<<<grid, 256, 0, st>>>(a, xq, xs);
-  return cudaGetLastError();
+  return launch_pdl(gather_fp8_kernel, dim3(grid), dim3(256), 0, st, a, xq, xs);
 }
 
 }  // namespace moe

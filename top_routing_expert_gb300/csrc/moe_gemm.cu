@@ -93,10 +93,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E;
 
-  for (int i = tid; i <= E; i += kGemmThreads) {
-    const int v = p.offsets[i];
-    offs[i] = v < 0 ? 0 : (v > p.rows ? p.rows : v);  // rows outside the buffer are never written
-  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
@@ -117,6 +113,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 3 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+  }
+  // the prologue above touches no global memory; the segment offsets and
+  // everything after may come from the previous kernel on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = tid; i <= E; i += kGemmThreads) {
+    const int v = p.offsets[i];
+    offs[i] = v < 0 ? 0 : (v > p.rows ? p.rows : v);  // rows outside the buffer are never written
   }
   __syncthreads();
   if (tid == 0)
@@ -312,8 +316,8 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<kBN><<<num_sms, kGemmThreads, smem, st>>>(tm_a, tm_b, a);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<kBN>, dim3(num_sms), dim3(kGemmThreads), smem, st, tm_a,
+                    tm_b, a);
 }
 
 }  // namespace moe

@@ -116,10 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
-  for (int i = tid; i <= E; i += kThreads) {
-    const int v = p.offsets[i];
-    offs[i] = v < 0 ? 0 : (v > p.rows ? p.rows : v);  // rows outside the buffer are never written
-  }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
     tmem_relinquish_pair();
@@ -141,6 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 3 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+  }
+  // the prologue above touches no global memory; the segment offsets and
+  // everything after may come from the previous kernel on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = tid; i <= E; i += kThreads) {
+    const int v = p.offsets[i];
+    offs[i] = v < 0 ? 0 : (v > p.rows ? p.rows : v);  // rows outside the buffer are never written
   }
   __syncthreads();
   if (tid == 0)
@@ -514,13 +518,17 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel on the stream finishes (the kernel
+  // waits for it before its first global access)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   err = cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<kFp8, kQOut, kGather>, tm_a, tm_b,
                            args);
   if (err != cudaSuccess) return err;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_gb300.h"
 
 namespace moe {
@@ -139,6 +141,27 @@ size_t gemm_smem_bytes(int E);
 
 cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, int E, int E_pad,
                                   cudaStream_t st);
+// Launches `kernel` on `st` with programmatic stream serialisation: its
+// CTAs may start, and run the prologue that touches no global memory, while
+// the previous kernel on the stream finishes (that kernel's
+// grid_launch_dependents()). Every kernel launched this way calls
+// grid_dependency_wait() before its first global access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int route_stages(int E_pad, int gate_mode);
 size_t route_smem_bytes(int E_pad, int stages, int gate_mode);
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,

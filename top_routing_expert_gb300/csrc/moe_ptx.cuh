@@ -21,6 +21,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel on its stream is still running. It calls
+// grid_dependency_wait() before it reads or writes any global memory (which
+// returns once the grids it depends on have completed and their writes are
+// visible; without such a dependency it returns at once), then
+// grid_launch_dependents() so that the next kernel may in turn start its
+// prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier ----
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -367,6 +367,8 @@ __device__ __forceinline__ void route_epilogue(const Src& src, const RouteArgs& 
 
 __global__ void gate_transpose_kernel(const uint16_t* __restrict__ gate,
                                       uint16_t* __restrict__ gateT, int H, int E, int E_pad) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t n = static_cast<int64_t>(E_pad) * H;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -453,7 +455,6 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   RouteSmem sm = carve_route_smem(smem + static_cast<size_t>(S) * stage_bytes, S, E32);
   const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(E32));
 
-  if (tile == 0 && tid == 0) *a.ticket = 0u;
   if (warp == 0) {
     tmem_alloc(sm.tmem_slot, ncols);
     tmem_relinquish();
@@ -471,6 +472,11 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_gate);
   }
+  // the prologue above touches no global memory; everything below may
+  // depend on the previous kernel on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (tile == 0 && tid == 0) *a.ticket = 0u;
   for (int i = tid; i < E32; i += blockDim.x)
     sm.bias_s[i] = (a.bias != nullptr && i < a.E) ? a.bias[i] : 0.f;
   for (int i = tid; i < 4 * E32; i += blockDim.x) sm.masks[i] = 0u;
@@ -611,7 +617,6 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
   const int n_epi = kTileTokens * L.npart;
   const uint32_t a_bytes = kTileTokens * kBlockK * 2;
 
-  if (blockIdx.x == 0 && tid == 0) *a.ticket = 0u;
   if (warp == 0) {
     tmem_alloc(tmem_slot, L.ncols);
     tmem_relinquish();
@@ -633,6 +638,11 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_gate);
   }
+  // the prologue above touches no global memory; everything below may
+  // depend on the previous kernel on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (blockIdx.x == 0 && tid == 0) *a.ticket = 0u;
   for (int i = tid; i < E32; i += blockDim.x)
     bias_s[i] = (a.bias != nullptr && i < a.E) ? a.bias[i] : 0.f;
   for (int i = tid; i < 4 * E32; i += blockDim.x) masks[i] = 0u;
@@ -764,6 +774,8 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1) route_logits_kernel(RouteA
   EpiScratch es = carve_epi(smem_raw, npart, KMAX);
   uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw + epi_scratch_bytes(npart, KMAX));
   float* red = reinterpret_cast<float*>(masks + 4 * E32);
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (tile == 0 && tid == 0) *a.ticket = 0u;
   for (int i = tid; i < 4 * E32; i += blockDim.x) masks[i] = 0u;
   __syncthreads();
@@ -781,6 +793,8 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
   const int tile = blockIdx.x;
   const int E32 = (a.E + 31) & ~31;
   uint32_t* masks = reinterpret_cast<uint32_t*>(smem_raw);
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (tile == 0 && tid == 0) *a.ticket = 0u;
   for (int i = tid; i < 4 * E32; i += kTileTokens) masks[i] = 0u;
   __syncthreads();
@@ -839,8 +853,7 @@ cudaError_t launch_gate_transpose(const uint16_t* gate, uint16_t* gateT, int H, 
   const int64_t n = static_cast<int64_t>(H) * E_pad;
   int blocks = static_cast<int>((n + 255) / 256);
   if (blocks > 4096) blocks = 4096;
-  gate_transpose_kernel<<<blocks, 256, 0, st>>>(gate, gateT, H, E, E_pad);
-  return cudaGetLastError();
+  return launch_pdl(gate_transpose_kernel, dim3(blocks), dim3(256), 0, st, gate, gateT, H, E, E_pad);
 }
 
 template <int KMAX>
@@ -856,8 +869,8 @@ cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_g
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  route_gemm_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(tm_x, tm_gate, a);
-  return cudaGetLastError();
+  return launch_pdl(route_gemm_kernel<KMAX>, dim3(a.n_tiles), dim3(kTileTokens * npart), smem, st,
+                    tm_x, tm_gate, a);
 }
 
 template <int KMAX>
@@ -870,9 +883,8 @@ cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap
                                          static_cast<int>(L.total));
   if (err != cudaSuccess) return err;
   const int grid = a.n_tiles < num_sms ? a.n_tiles : num_sms;
-  route_persistent_kernel<KMAX><<<grid, kTileTokens + kTileTokens * L.npart, L.total, st>>>(
-      tm_x, tm_gate, a);
-  return cudaGetLastError();
+  return launch_pdl(route_persistent_kernel<KMAX>, dim3(grid),
+                    dim3(kTileTokens + kTileTokens * L.npart), L.total, st, tm_x, tm_gate, a);
 }
 
 bool route_use_persistent(const RouteArgs& a, int num_sms) {
@@ -902,8 +914,8 @@ cudaError_t launch_route_logits_k(const RouteArgs& a, cudaStream_t st) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  route_logits_kernel<KMAX><<<a.n_tiles, kTileTokens * npart, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(route_logits_kernel<KMAX>, dim3(a.n_tiles), dim3(kTileTokens * npart), smem, st,
+                    a);
 }
 
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
@@ -915,8 +927,7 @@ cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st) {
 
 cudaError_t launch_rank(const RankArgs& a, cudaStream_t st) {
   const int E32 = (a.E + 31) & ~31;
-  rank_kernel<<<a.n_tiles, kTileTokens, 4 * 4 * E32, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(rank_kernel, dim3(a.n_tiles), dim3(kTileTokens), 4 * 4 * E32, st, a);
 }
 
 }  // namespace moe
