@@ -216,3 +216,53 @@ def test_ep_per_rank_capacity_equals_each_shard_alone():
         ref = O.token_outputs(np64(inp["x"][sh]), gidx, rr.w, dp.dest_row >= 0,
                               np64(inp["W1"]), np64(inp["W2"]))
         assert_ffn_close(np64(y_ep[sh]), ref, f"per-rank capacity rank {r}")
+
+
+DRIVER_CHILD = r"""
+import json, os, sys
+sys.path.insert(0, ROOT)
+import torch, torch.distributed as dist
+import top_routing_expert_gb300 as moe
+from top_routing_expert_gb300.ep import ExpertParallelMoE
+import workloads as W
+moe.build(); moe.load_library()
+torch.cuda.set_device(0)
+dist.init_process_group("nccl", init_method="tcp://127.0.0.1:PORT", rank=0, world_size=1)
+out = {}
+for cap in ("global", "per_rank"):
+    w = W.custom(2048, 256, 8, 2, 384, 0.8, "zipf", name="ep_driver")
+    inp = W.make_inputs(w, seed=9)
+    d = {n: (v.cuda() if v is not None else None) for n, v in inp.items()}
+    layer = ExpertParallelMoE(w.T, w.H, w.E, w.k, w.h, w.cf, capacity=cap)
+    y = layer.forward(d["x"], d["gate"], d["bias"], d["W1"], d["W2"])
+    s = moe.MoeShape.make(w.T, w.H, w.E, w.k, w.h, w.cf)
+    y_ref = torch.empty_like(y)
+    moe.moe_layer_fwd(s, d["x"], d["gate"], d["bias"], d["W1"], d["W2"], y_ref,
+                      ws=moe.Workspace(s))
+    torch.cuda.synchronize()
+    out[cap] = {"equal": bool(torch.equal(y, y_ref)), "status": int(layer.status.item())}
+dist.destroy_process_group()
+print(json.dumps(out))
+"""
+
+
+def test_ep_driver_on_a_one_rank_group_equals_the_layer():
+    """The driver (top_routing_expert_gb300.ep) with every collective issued
+    for real on a one-rank NCCL group: all experts are local, so both
+    capacity modes must give moe_layer_fwd's bits."""
+    import json
+    import os
+    import socket
+    import subprocess
+    import sys
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = DRIVER_CHILD.replace("ROOT", repr(root)).replace("PORT", str(port))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600,
+                       env=dict(os.environ, NCCL_NVLS_ENABLE="0"))
+    assert r.returncode == 0, r.stderr[-3000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    for cap, res in out.items():
+        assert res["status"] == 0 and res["equal"], (cap, res)

@@ -131,16 +131,17 @@ class ExpertParallelMoE:
         recv_sizes = [sum(r) for r in recv_counts.tolist()]
         x_recv = exchange_rows(self.x_perm, send_sizes, recv_sizes, self.group)
         n = x_recv.shape[0]
-        x_loc = torch.empty_like(x_recv)
-        local_off = torch.zeros(E_loc + 1, dtype=torch.int32, device=self.dev)
-        moe_ep_regroup(world, E_loc, recv_counts, x_recv, x_loc, True, local_off)
-        act = torch.empty((n, h), dtype=torch.bfloat16, device=self.dev)
-        y_loc = torch.empty_like(x_loc)
-        ffn_shape = MoeShape.make(n, H, E_loc, 1, h, 1.0)
-        moe_expert_ffn(ffn_shape, x_loc, local_off, W1_local, W2_local, act, y_loc,
-                       dev_status=self.status)
-        y_send = torch.empty_like(y_loc)
-        moe_ep_regroup(world, E_loc, recv_counts, y_loc, y_send, False)
+        y_send = torch.empty_like(x_recv)
+        if n > 0:   # a rank whose experts received nothing has no FFN to run
+            x_loc = torch.empty_like(x_recv)
+            local_off = torch.zeros(E_loc + 1, dtype=torch.int32, device=self.dev)
+            moe_ep_regroup(world, E_loc, recv_counts, x_recv, x_loc, True, local_off)
+            act = torch.empty((n, h), dtype=torch.bfloat16, device=self.dev)
+            y_loc = torch.empty_like(x_loc)
+            ffn_shape = MoeShape.make(n, H, E_loc, 1, h, 1.0)
+            moe_expert_ffn(ffn_shape, x_loc, local_off, W1_local, W2_local, act, y_loc,
+                           dev_status=self.status)
+            moe_ep_regroup(world, E_loc, recv_counts, y_loc, y_send, False)
         exchange_rows(y_send, recv_sizes, send_sizes, self.group, out=self.y_perm)
         moe_combine(s, self.y_perm, self.dest, self.w, y)
         return y
