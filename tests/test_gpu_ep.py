@@ -242,7 +242,7 @@ for cap in ("global", "per_rank"):
     torch.cuda.synchronize()
     out[cap] = {"equal": bool(torch.equal(y, y_ref)), "status": int(layer.status.item())}
 dist.destroy_process_group()
-print(json.dumps(out))
+print("EP_RESULT " + json.dumps(out), flush=True)
 """
 
 
@@ -263,6 +263,9 @@ def test_ep_driver_on_a_one_rank_group_equals_the_layer():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600,
                        env=dict(os.environ, NCCL_NVLS_ENABLE="0"))
     assert r.returncode == 0, r.stderr[-3000:]
-    out = json.loads(r.stdout.strip().splitlines()[-1])
+    # NCCL may print its own lines to stdout too, in either order
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("EP_RESULT ")]
+    assert len(lines) == 1, r.stdout[-3000:]
+    out = json.loads(lines[0][len("EP_RESULT "):])
     for cap, res in out.items():
         assert res["status"] == 0 and res["equal"], (cap, res)

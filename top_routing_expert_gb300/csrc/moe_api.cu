@@ -236,6 +236,24 @@ bool tmap_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t oute
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A bf16 row-major matrix [rows, K] (K % 64 == 0) seen as 64-element
+// k-blocks: 3-D {64, rows, K/64}, the k-block dimension 128 bytes apart, read
+// in boxes of box_rows rows x kbps consecutive k-blocks. A box lands in shared
+// memory k-block by k-block, each the box_rows x 128-byte swizzled tile that
+// a 2-D {64, box_rows} box would give.
+bool tmap_bf16_kblocks(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows,
+                       uint32_t box_rows, int kbps) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t gdim[3] = {64, rows, K / 64};
+  const cuuint64_t gstride[2] = {K * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(kbps)};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A byte (e4m3) row-major matrix [outer, inner] in 128 x 128 boxes (one
 // 128-byte swizzle row of K per box row); inner must be a multiple of 16.
 bool tmap_u8_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
@@ -301,19 +319,23 @@ moe_status run_route(const Dims& d, const moe_bf16* x, const moe_bf16* gate, con
     MOE_CUDA(launch_route_logits(a, st));
   } else {
     CUtensorMap tm_x, tm_g;
-    if (!tmap_bf16_2d(&tm_x, x, d.H, d.T, kBlockK, kTileTokens)) return MOE_ERR_CUDA;
     // The gate [H,E] is the UMMA's B operand as given (MN-major TMA boxes of
     // 64 experts) when E >= 64 and its rows are 16-byte multiples; otherwise
     // a transposed, padded copy [E_pad,H] is made in the workspace first.
-    if (d.E >= 64 && d.E % 8 == 0 && tmap_bf16_2d(&tm_g, gate, d.E, d.H, 64, kBlockK)) {
-      a.gate_mode = kGateMnMajor;
-    } else {
+    const int sms = num_sms();
+    a.gate_mode = (d.E >= 64 && d.E % 8 == 0) ? kGateMnMajor : kGateTransposed;
+    route_plan(a, sms);
+    if (a.gate_mode == kGateMnMajor &&
+        !tmap_bf16_2d(&tm_g, gate, d.E, d.H, 64, static_cast<uint32_t>(kBlockK * a.kbps))) {
       a.gate_mode = kGateTransposed;
-      MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
-      if (!tmap_bf16_2d(&tm_g, w.gateT, d.H, d.E_pad, kBlockK, d.E_pad)) return MOE_ERR_CUDA;
+      route_plan(a, sms);
     }
-    a.stages = route_stages(d.E_pad, a.gate_mode);
-    MOE_CUDA(launch_route_gemm(tm_x, tm_g, a, st, num_sms()));
+    if (a.gate_mode == kGateTransposed) {
+      MOE_CUDA(launch_gate_transpose(gate, w.gateT, d.H, d.E, d.E_pad, st));
+      if (!tmap_bf16_kblocks(&tm_g, w.gateT, d.H, d.E_pad, d.E_pad, a.kbps)) return MOE_ERR_CUDA;
+    }
+    if (!tmap_bf16_kblocks(&tm_x, x, d.H, d.T, kTileTokens, a.kbps)) return MOE_ERR_CUDA;
+    MOE_CUDA(launch_route_gemm(tm_x, tm_g, a, st, sms));
   }
   return MOE_OK;
 }
@@ -413,6 +435,9 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.d_scale = nullptr;
   g.a_rows = a_rows;
   g.a_src_rows = a_src_rows;
+  g.stages = 0;
+  g.group = 0;
+  g.a_hint = kAHintLast;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   if (d.A >= kPairGemmMinRows || a_rows != nullptr)
@@ -448,6 +473,9 @@ moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
   g.d_scale = d_scale;
   g.a_rows = nullptr;
   g.a_src_rows = 0;
+  g.stages = 0;
+  g.group = 0;
+  g.a_hint = kAHintLast;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   MOE_CUDA(launch_grouped_gemm_pair_fp8(tm_a, tm_b, g, num_sms(), st));

@@ -39,7 +39,8 @@ constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 // pair m-tiles (4096 rows), so that a group stays within one expert's weights
 // (1.7 % faster on the power-capped large-expert layer, whose DRAM traffic it
 // lowers); 8 for smaller or ragged experts (0.5-0.8 % faster there).
-__device__ __forceinline__ int raster_group(int total_pm, int E) {
+__device__ __forceinline__ int raster_group(int total_pm, int E, int forced) {
+  if (forced > 0) return forced;
   return total_pm >= 16 * E ? 16 : 8;
 }
 
@@ -48,8 +49,9 @@ struct PairTile {
 };
 
 __device__ __forceinline__ PairTile decode_pair(int L, const int* pm_prefix, const int* offs,
-                                                int E, int total_pm, int n_tiles_n, int rank) {
-  const int group = raster_group(total_pm, E);
+                                                int E, int total_pm, int n_tiles_n, int rank,
+                                                int forced_group) {
+  const int group = raster_group(total_pm, E, forced_group);
   const int per_group = group * n_tiles_n;
   const int g = L / per_group;
   const int first = g * group;
@@ -199,11 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool aborted = false;
-      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_last = l2_policy_evict_last();
+      const uint64_t pol_first = l2_policy_evict_first();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
-        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
         const int b_row = c.e * p.K;
         const int b_col = c.n0 + static_cast<int>(rank) * (kBN / 2);
+        const uint64_t pol_a =
+            (p.a_hint == kAHintLastDemote && c.n0 / kBN == n_tiles_n - 1) ? pol_first : pol_last;
         int gr[4] = {0, 0, 0, 0};
         if constexpr (kGather) {
 #pragma unroll
@@ -226,8 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sb = sa + kABytes;
           if (lane == 0) {
             if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
-            // A rows are reused by every n-tile of the group: keep them in L2
-            if constexpr (!kGather) tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
+            // A rows are reused by every n-tile of the group
+            if constexpr (!kGather) {
+              if (p.a_hint == kAHintNormal)
+                tma_load_2d_pair(sa, &tm_a, bar, kb * kKE, c.row0);
+              else
+                tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
+            }
             if constexpr (kFp8) {
               // B^T [E*N, K] e4m3: this CTA's 128 output columns as K-major rows
               tma_load_2d_pair(sb, &tm_b, bar, kb * kKE, c.e * p.N + b_col);
@@ -350,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = cluster; L < total; L += n_clusters) {
-      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
       const int row = c.row0 + 32 * q + lane;
       const bool valid = row < c.row_end;
       const int col0 = c.n0 + half * (kBN / 2);

@@ -22,6 +22,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;      // waits for in-flight cop
 // Router epilogue arguments (GEMM and logits entry points).
 struct RouteArgs {
   int T, H, E, E_pad, k, n_tiles, stages;
+  int kbps;                // 64-deep k-blocks per pipeline stage (1, 2 or 4; divides H/64)
   int gate_mode;           // how the gate reaches shared memory (kGate* below)
   const float* bias;       // [E] or nullptr (GEMM path only)
   const float* noise_u;    // [T,E] uniforms in [0,1) for Gumbel noise, or nullptr
@@ -114,9 +115,17 @@ struct GemmArgs {
   const int32_t* a_rows;   // optional: A row r is row a_rows[r] of the A tensor (a gather,
   int a_src_rows;          //   by TMA, from a tensor of a_src_rows rows); CTA-pair kernel
   int stages;              // CTA-pair kernel: pipeline depth (set by its launcher)
+  int group;               // CTA-pair kernel: pair m-tiles per raster group (0: by size)
+  int a_hint;              // CTA-pair kernel: L2 priority of A loads (kAHint* below)
   uint32_t* dev_status;
   uint64_t timeout_ns;
 };
+
+// L2 eviction priority the CTA-pair GEMM gives its A (row-panel) loads:
+// normal; evict-last (kept for the group's other n-tiles); or evict-last
+// except on the last n-tile of a group, whose loads mark the lines
+// evict-first again, so that finished groups do not keep L2 from later ones.
+enum { kAHintNormal = 0, kAHintLast = 1, kAHintLastDemote = 2 };
 
 // How the router's B operand (the gate, N = E_pad experts x K = H) reaches
 // each pipeline stage:
@@ -131,10 +140,17 @@ struct GemmArgs {
 //                     (large-expert router 76 -> 93 us on GB300).
 enum { kGateTransposed = 0, kGateMnMajor = 1 };
 
-// Shared-memory bytes of the gate per 64-deep k-block stage.
+// Shared-memory bytes of the gate per 64-deep k-block.
 __host__ __device__ inline uint32_t route_gate_stage_bytes(int E_pad, int gate_mode) {
   return gate_mode == kGateMnMajor ? static_cast<uint32_t>((E_pad + 63) / 64) * 8192u
                                    : static_cast<uint32_t>(E_pad) * kBlockK * 2;
+}
+
+// Shared-memory bytes of one router pipeline stage of `kbps` k-blocks: the
+// tile's 128 rows of x and the gate's rows for those k-blocks.
+__host__ __device__ inline uint32_t route_stage_bytes(int E_pad, int gate_mode, int kbps) {
+  return static_cast<uint32_t>(kbps) *
+         (static_cast<uint32_t>(kTileTokens * kBlockK * 2) + route_gate_stage_bytes(E_pad, gate_mode));
 }
 
 size_t gemm_smem_bytes(int E);
@@ -162,8 +178,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-int route_stages(int E_pad, int gate_mode);
-size_t route_smem_bytes(int E_pad, int stages, int gate_mode);
+// Sets a.kbps and a.stages for the router kernel launch_route_gemm will run
+// (a.E, a.E_pad, a.H, a.k, a.n_tiles and a.gate_mode set).
+void route_plan(RouteArgs& a, int num_sms);
+size_t route_smem_bytes(int E_pad, int stages, int gate_mode, int kbps);
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
                               const RouteArgs& a, cudaStream_t st, int num_sms);
 cudaError_t launch_route_logits(const RouteArgs& a, cudaStream_t st);

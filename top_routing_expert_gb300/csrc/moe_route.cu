@@ -378,27 +378,52 @@ __global__ void gate_transpose_kernel(const uint16_t* __restrict__ gate,
   }
 }
 
-// The gate's part of one pipeline stage (k rows kb*64 .. kb*64+63): one box
-// of the transposed gate [E_pad, H], or ceil(E_pad/64) boxes of 64 expert
-// columns of the gate [H, E] as given (inner coordinate a multiple of 64
-// elements, so every box starts on a 128-byte boundary).
-__device__ __forceinline__ void load_gate_stage(uint8_t* dst, const CUtensorMap* tm_gate,
-                                                uint64_t* bar, int kb, const RouteArgs& a) {
+// A pipeline stage holds a.kbps consecutive 64-deep k-blocks (kb0 ..
+// kb0+kbps-1): first x, one 3-D TMA box of 128 rows x 64 k x kbps k-blocks
+// (k-block r at r * 16 KB, the K-major 128-byte-swizzled layout per
+// k-block), then the gate. Fewer, larger copies keep more of x in flight
+// per instruction: streaming 512 MB through 152 SMs with 64 KB copies ran
+// 25 % faster than with 16 KB ones on GB300.
+//
+// The gate's part: one 3-D box of the transposed gate [E_pad, H] (k-block
+// r's E_pad rows at r * E_pad * 128 bytes), or ceil(E_pad/64) boxes of 64
+// expert columns x 64*kbps k rows of the gate [H, E] as given (column block
+// cb at cb * kbps * 8 KB, k-block r at r * 8 KB inside it; the inner
+// coordinate is a multiple of 64 elements, so every box starts on a
+// 128-byte boundary).
+__device__ __forceinline__ void load_route_stage(uint8_t* dst, const CUtensorMap* tm_x,
+                                                 const CUtensorMap* tm_gate, uint64_t* bar,
+                                                 int tile, int kb0, const RouteArgs& a) {
+  tma_load_3d(dst, tm_x, bar, 0, tile * kTileTokens, kb0);
+  uint8_t* g = dst + static_cast<size_t>(a.kbps) * kTileTokens * kBlockK * 2;
   if (a.gate_mode == kGateMnMajor) {
     for (int cb = 0; cb < (a.E_pad + 63) / 64; ++cb)
-      tma_load_2d(dst + 8192 * cb, tm_gate, bar, 64 * cb, kb * kBlockK);
+      tma_load_2d(g + 8192 * a.kbps * cb, tm_gate, bar, 64 * cb, kb0 * kBlockK);
   } else {
-    tma_load_2d(dst, tm_gate, bar, kb * kBlockK, 0);
+    tma_load_3d(g, tm_gate, bar, 0, 0, kb0);
   }
 }
 
-// UMMA descriptors of the gate (the B operand, N = E_pad) for the kk-th
-// 16-deep K step of a stage: K-major 128-byte rows (32 bytes per step), or
-// MN-major 128-byte rows of 64 experts, one per k (16 rows = 2 KB per step,
-// 64-column blocks 8 KB apart).
-__device__ __forceinline__ uint64_t route_gate_desc(uint32_t b_addr, int kk, int gate_mode) {
-  return gate_mode == kGateMnMajor ? smem_desc_sw128(b_addr + 2048u * kk, 8192u, 1024u)
-                                   : smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
+// The UMMAs of one stage: D[128 x E_pad] (+)= X[128 x 64] * gate^T[64 x
+// E_pad] for each of its k-blocks, 16-deep K steps. Gate descriptors:
+// K-major 128-byte rows (32 bytes per step), or MN-major 128-byte rows of 64
+// experts, one per k (16 rows = 2 KB per step, column blocks kbps * 8 KB
+// apart).
+__device__ __forceinline__ void route_stage_mma(uint32_t d_tmem, uint32_t stage_addr,
+                                                uint32_t idesc, bool first, const RouteArgs& a) {
+  const uint32_t b_addr = stage_addr + static_cast<uint32_t>(a.kbps) * kTileTokens * kBlockK * 2;
+  for (int r = 0; r < a.kbps; ++r) {
+#pragma unroll
+    for (int kk = 0; kk < kBlockK / 16; ++kk) {
+      const uint64_t ad = smem_desc_sw128(stage_addr + 16384u * r + 32u * kk, 16u, 1024u);
+      const uint64_t bd =
+          a.gate_mode == kGateMnMajor
+              ? smem_desc_sw128(b_addr + 8192u * r + 2048u * kk, 8192u * a.kbps, 1024u)
+              : smem_desc_sw128(b_addr + static_cast<uint32_t>(a.E_pad) * 128u * r + 32u * kk,
+                                16u, 1024u);
+      umma_bf16(d_tmem, ad, bd, idesc, (first && (r | kk) == 0) ? 0u : 1u);
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t route_idesc(const RouteArgs& a) {
@@ -434,9 +459,8 @@ __device__ __forceinline__ RouteSmem carve_route_smem(uint8_t* p, int stages, in
 }
 
 // One CTA per 128-token tile; the launcher picks this kernel when there are
-// no more tiles than SMs (the persistent kernel takes larger batches).
-// Stages are sized so that two CTAs could share an SM; with one CTA per SM,
-// up to 8 stages measured the same on the fine-grained router (46 us).
+// no more tiles than SMs (the persistent kernel takes larger batches), so
+// one CTA per SM and a stage ring of up to ~200 KB.
 template <int KMAX>
 __global__ void __launch_bounds__(kTileTokens * 8, 1)
     route_gemm_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -449,9 +473,7 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   const int npart = route_parts_of(a.E), cpt = route_cpt_of(a.E);
   const int ecols = npart * cpt;                // columns the epilogue reads (>= E)
   const int E32 = ((ecols > a.E_pad ? ecols : a.E_pad) + 31) & ~31;
-  const uint32_t a_bytes = kTileTokens * kBlockK * 2;
-  const uint32_t b_bytes = route_gate_stage_bytes(a.E_pad, a.gate_mode);
-  const uint32_t stage_bytes = a_bytes + b_bytes;
+  const uint32_t stage_bytes = route_stage_bytes(a.E_pad, a.gate_mode, a.kbps);
   RouteSmem sm = carve_route_smem(smem + static_cast<size_t>(S) * stage_bytes, S, E32);
   const uint32_t ncols = static_cast<uint32_t>(route_tmem_cols(E32));
 
@@ -485,41 +507,33 @@ __global__ void __launch_bounds__(kTileTokens * 8, 1)
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_slot;
   const WaitCtl wc{sm.abort_flag, a.dev_status, a.timeout_ns};
-  const int nk = a.H / kBlockK;
+  const int ns = a.H / (kBlockK * a.kbps);  // stages per tile
 
   if (warp == 0 && lane == 0) {
-    // TMA producer: the tile's 128 rows x 64 k of x and the gate's k-block
-    // per stage (an L2 prefetch of whole 512-byte row pieces ahead of these
-    // loads measured 2-8 % slower and was dropped)
-    int kb = 0;
-    for (; kb < nk; ++kb) {
-      const int s = kb % S;
-      if (kb >= S && !mbar_wait(&sm.empty[s], ((kb / S) - 1) & 1, wc)) break;
-      uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+    // TMA producer (an L2 prefetch of whole 512-byte row pieces ahead of
+    // these loads measured 2-8 % slower and was dropped)
+    int i = 0;
+    for (; i < ns; ++i) {
+      const int s = i % S;
+      if (i >= S && !mbar_wait(&sm.empty[s], ((i / S) - 1) & 1, wc)) break;
       mbar_arrive_expect_tx(&sm.full[s], stage_bytes);
-      tma_load_2d(st, &tm_x, &sm.full[s], kb * kBlockK, tile * kTileTokens);
-      load_gate_stage(st + a_bytes, &tm_gate, &sm.full[s], kb, a);
+      load_route_stage(smem + static_cast<size_t>(s) * stage_bytes, &tm_x, &tm_gate, &sm.full[s],
+                       tile, i * a.kbps, a);
     }
-    if (kb < nk) {
+    if (i < ns) {
       // aborted: let the loads already issued land before the CTA exits
-      for (int d = (kb > S ? kb - S : 0); d < kb; ++d)
+      for (int d = (i > S ? i - S : 0); d < i; ++d)
         mbar_wait_drain(&sm.full[d % S], (d / S) & 1, kDrainLimitNs);
     }
   } else if (warp == 1 && lane == 0) {
-    // UMMA issuer: D[128 x E_pad] += X[128 x 64] * gate^T[64 x E_pad] per stage
+    // UMMA issuer
     const uint32_t idesc = route_idesc(a);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % S;
-      if (!mbar_wait(&sm.full[s], (kb / S) & 1, wc)) break;
+    for (int i = 0; i < ns; ++i) {
+      const int s = i % S;
+      if (!mbar_wait(&sm.full[s], (i / S) & 1, wc)) break;
       tc_fence_after();
-      const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
-      const uint32_t b_addr = a_addr + a_bytes;
-#pragma unroll
-      for (int kk = 0; kk < kBlockK / 16; ++kk) {
-        const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-        umma_bf16(tmem, ad, route_gate_desc(b_addr, kk, a.gate_mode), idesc,
-                  (kb | kk) != 0 ? 1u : 0u);
-      }
+      route_stage_mma(tmem, smem_u32(smem + static_cast<size_t>(s) * stage_bytes), idesc, i == 0,
+                      a);
       umma_commit(&sm.empty[s]);
     }
     umma_commit(sm.done);
@@ -572,13 +586,14 @@ struct PersistLayout {
   size_t off_bar, off_bias, off_masks, off_red, off_epi, total;
 };
 
-__host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int kmax, int gate_mode) {
+__host__ __device__ inline PersistLayout persist_layout(int E, int E_pad, int kmax, int gate_mode,
+                                                        int kbps) {
   PersistLayout L;
   L.npart = persist_parts_of(E);
   L.cpt = persist_cpt_of(E);
   const int ecols = L.npart * L.cpt;
   L.E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
-  L.stage_bytes = static_cast<uint32_t>(kTileTokens * kBlockK * 2) + route_gate_stage_bytes(E_pad, gate_mode);
+  L.stage_bytes = route_stage_bytes(E_pad, gate_mode, kbps);
   int c = 32;
   while (c < 2 * L.E32) c <<= 1;
   L.ncols = static_cast<uint32_t>(c);
@@ -601,7 +616,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode);
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode, a.kbps);
   const int S = L.S, E32 = L.E32;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   uint64_t* empty = full + S;
@@ -615,7 +630,6 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
   float* red = reinterpret_cast<float*>(smem + L.off_red);
   const EpiScratch es = carve_epi(smem + L.off_epi, L.npart, KMAX);
   const int n_epi = kTileTokens * L.npart;
-  const uint32_t a_bytes = kTileTokens * kBlockK * 2;
 
   if (warp == 0) {
     tmem_alloc(tmem_slot, L.ncols);
@@ -651,7 +665,7 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, a.dev_status, a.timeout_ns};
-  const int nk = a.H / kBlockK;
+  const int ns = a.H / (kBlockK * a.kbps);  // stages per tile
 
   if (warp == 0) {
     if (lane == 0) {
@@ -661,15 +675,14 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
       int issued = 0;
       bool aborted = false;
       for (int tile = blockIdx.x; tile < a.n_tiles && !aborted; tile += gridDim.x) {
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int i = 0; i < ns; ++i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             aborted = true;
             break;
           }
-          uint8_t* st = smem + static_cast<size_t>(stage) * L.stage_bytes;
           mbar_arrive_expect_tx(&full[stage], L.stage_bytes);
-          tma_load_2d(st, &tm_x, &full[stage], kb * kBlockK, tile * kTileTokens);
-          load_gate_stage(st + a_bytes, &tm_gate, &full[stage], kb, a);
+          load_route_stage(smem + static_cast<size_t>(stage) * L.stage_bytes, &tm_x, &tm_gate,
+                           &full[stage], tile, i * a.kbps, a);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -702,20 +715,14 @@ __global__ void __launch_bounds__(kTileTokens + kTileTokens * kPersistParts, 1)
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * E32);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int i = 0; i < ns; ++i) {
           if (!mbar_wait(&full[stage], phase, wc)) {
             aborted = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(stage) * L.stage_bytes);
-          const uint32_t b_addr = a_addr + a_bytes;
-#pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-            umma_bf16(d_tmem, ad, route_gate_desc(b_addr, kk, a.gate_mode), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
-          }
+          route_stage_mma(d_tmem, smem_u32(smem + static_cast<size_t>(stage) * L.stage_bytes),
+                          idesc, i == 0, a);
           umma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
@@ -832,19 +839,11 @@ __global__ void __launch_bounds__(kTileTokens) rank_kernel(RankArgs a) {
 
 // ------------------------------------------------------------------ host ----
 
-int route_stages(int E_pad, int gate_mode) {
-  // the per-tile kernel runs with at most one CTA per SM (no more tiles
-  // than SMs): as many stages as fit in ~200 KB
-  const int stage = kTileTokens * kBlockK * 2 + static_cast<int>(route_gate_stage_bytes(E_pad, gate_mode));
-  int s = (200 * 1024) / stage;
-  return s < 2 ? 2 : (s > 10 ? 10 : s);
-}
-
-size_t route_smem_bytes(int E_pad, int stages, int gate_mode) {
+size_t route_smem_bytes(int E_pad, int stages, int gate_mode, int kbps) {
   const int E = E_pad;  // upper bound for the epilogue's column span
   const int ecols = route_parts_of(E) * route_cpt_of(E);
   const int E32 = ((ecols > E_pad ? ecols : E_pad) + 31) & ~31;
-  const size_t stage = static_cast<size_t>(kTileTokens) * kBlockK * 2 + route_gate_stage_bytes(E_pad, gate_mode);
+  const size_t stage = route_stage_bytes(E_pad, gate_mode, kbps);
   return 1024 + stage * stages + 8 * (2 * stages + 1) + 16 + 4 * E32 + 2 * 4 * 4 * E32;
 }
 
@@ -861,10 +860,10 @@ cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_g
                                 const RouteArgs& a, cudaStream_t st) {
   const int npart = route_parts_of(a.E);
   // the epilogue scratch lives in the pipeline stages once they are free
-  const size_t stage_area = static_cast<size_t>(a.stages) *
-                            (static_cast<size_t>(kTileTokens) * kBlockK * 2 + route_gate_stage_bytes(a.E_pad, a.gate_mode));
+  const size_t stage_area =
+      static_cast<size_t>(a.stages) * route_stage_bytes(a.E_pad, a.gate_mode, a.kbps);
   if (epi_scratch_bytes(npart, KMAX) > stage_area) return cudaErrorInvalidConfiguration;
-  const size_t smem = route_smem_bytes(a.E_pad, a.stages, a.gate_mode);
+  const size_t smem = route_smem_bytes(a.E_pad, a.stages, a.gate_mode, a.kbps);
   cudaError_t err = cudaFuncSetAttribute(route_gemm_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -876,7 +875,7 @@ cudaError_t launch_route_gemm_k(const CUtensorMap& tm_x, const CUtensorMap& tm_g
 template <int KMAX>
 cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
                                       const RouteArgs& a, int num_sms, cudaStream_t st) {
-  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode);
+  const PersistLayout L = persist_layout(a.E, a.E_pad, KMAX, a.gate_mode, a.kbps);
   if (L.S < 2) return cudaErrorInvalidConfiguration;
   cudaError_t err = cudaFuncSetAttribute(route_persistent_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -889,6 +888,29 @@ cudaError_t launch_route_persistent_k(const CUtensorMap& tm_x, const CUtensorMap
 
 bool route_use_persistent(const RouteArgs& a, int num_sms) {
   return a.n_tiles > num_sms;
+}
+
+// k-blocks per stage: 4, 2 or 1, the largest that divides H/64 and leaves at
+// least two stages in the kernel's ring; the per-tile kernel then takes as
+// many stages as fit in ~200 KB (at most 10).
+void route_plan(RouteArgs& a, int num_sms) {
+  const int nk = a.H / kBlockK;
+  const int kmax = a.k <= 2 ? 2 : a.k <= 4 ? 4 : a.k <= 6 ? 6 : 8;
+  const bool persistent = route_use_persistent(a, num_sms);
+  constexpr int kRing = 200 * 1024;
+  for (int r = 4; r >= 1; r >>= 1) {
+    if (nk % r != 0) continue;
+    a.kbps = r;
+    const bool fits =
+        persistent ? persist_layout(a.E, a.E_pad, kmax, a.gate_mode, r).S >= 2
+                   : kRing / static_cast<int>(route_stage_bytes(a.E_pad, a.gate_mode, r)) >= 2;
+    if (fits) break;
+  }
+  a.stages = 0;
+  if (!persistent) {
+    const int s = kRing / static_cast<int>(route_stage_bytes(a.E_pad, a.gate_mode, a.kbps));
+    a.stages = s < 2 ? 2 : (s > 10 ? 10 : s);
+  }
 }
 
 cudaError_t launch_route_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_gate,
