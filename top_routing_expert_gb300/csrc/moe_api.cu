@@ -254,6 +254,21 @@ bool tmap_bf16_kblocks(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per-expert bf16 matrices W [E][K][N] (row-major, N % 64 == 0) seen as
+// 3-D {N, K, E}, read in boxes of 64 columns x box_k rows of one expert.
+bool tmap_bf16_experts(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t K, uint64_t E,
+                       uint32_t box_k) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t gdim[3] = {N, K, E};
+  const cuuint64_t gstride[2] = {N * 2, N * K * 2};
+  const cuuint32_t box[3] = {64, box_k, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A byte (e4m3) row-major matrix [outer, inner] in 128 x 128 boxes (one
 // 128-byte swizzle row of K per box row); inner must be a multiple of 16.
 bool tmap_u8_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
@@ -414,12 +429,23 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
                     const int32_t* a_rows = nullptr, int a_src_rows = 0) {
   if (d.A == 0) return MOE_OK;
   CUtensorMap tm_a, tm_b;
+  const bool pair = d.A >= kPairGemmMinRows || a_rows != nullptr;
   if (a_rows != nullptr) {
     if (!tmap_bf16_2d(&tm_a, A, K, a_src_rows, kBlockK, 1)) return MOE_ERR_CUDA;
+  } else if (pair) {
+    // the CTA-pair kernel's stages hold two k-blocks of its 128 rows
+    if (!tmap_bf16_kblocks(&tm_a, A, K, d.A, 128, 2)) return MOE_ERR_CUDA;
   } else if (!tmap_bf16_2d(&tm_a, A, K, d.A, kBlockK, 128)) {
     return MOE_ERR_CUDA;
   }
-  if (!tmap_bf16_2d(&tm_b, W, N, static_cast<uint64_t>(d.E) * K, 64, kBlockK)) return MOE_ERR_CUDA;
+  if (pair) {
+    // W [E][K][N] in boxes of 64 columns x 64 (gathered A) or 128 k-rows of one
+    // expert: rows past K read as zeros
+    if (!tmap_bf16_experts(&tm_b, W, N, K, d.E, a_rows != nullptr ? kBlockK : 2 * kBlockK))
+      return MOE_ERR_CUDA;
+  } else if (!tmap_bf16_2d(&tm_b, W, N, static_cast<uint64_t>(d.E) * K, 64, kBlockK)) {
+    return MOE_ERR_CUDA;
+  }
   GemmArgs g;
   g.offsets = offsets;
   g.E = d.E;
@@ -440,7 +466,7 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.a_hint = kAHintLast;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
-  if (d.A >= kPairGemmMinRows || a_rows != nullptr)
+  if (pair)
     MOE_CUDA(launch_grouped_gemm_pair(tm_a, tm_b, g, num_sms(), st));
   else
     MOE_CUDA(launch_grouped_gemm(tm_a, tm_b, g, num_sms(), st));

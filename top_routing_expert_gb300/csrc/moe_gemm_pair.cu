@@ -1,9 +1,17 @@
 // Grouped GEMM over ragged expert segments, CTA-pair version: the same
 // product as grouped_gemm_kernel (D[r,:] = A[r,:] . B[e(r)], optional GELU)
 // with a 2-CTA UMMA (cta_group::2, M=256, N=256). Each CTA of a cluster pair
-// holds its own 128 rows of A and its own 128 columns of B per stage, so a
-// stage is 32 KB instead of 48 KB: six or seven stages fit, and shared
-// memory moves a third less data per FLOP than the single-CTA kernel.
+// holds its own 128 rows of A and its own 128 columns of B per 64-deep
+// k-block, 32 KB instead of 48 KB, so shared memory moves a third less data
+// per FLOP than the single-CTA kernel. In the bf16 kernel that loads A by
+// tile, a pipeline stage holds two k-blocks (64 KB, three stages): A as one
+// 3-D TMA box of 128 rows x 2 k-blocks, B as two boxes of 64 columns x 128
+// k-rows. On the power-capped large-expert layer this took GEMM1 from 0.81
+// to 0.89 and GEMM2 from 0.87 to 0.92 of the measured burst peak on GB300
+// against one k-block per 32 KB stage (seven stages): half as many stage
+// hand-offs and barrier waits for the same bytes. The FP8 kernel's stages
+// hold two 128-deep k-blocks as one 2-D box each of A and B; the
+// gathered-A kernel keeps one k-block per stage.
 //
 // A pair tile is (expert e, pair index pm, n-tile): CTA rank r computes the
 // expert's local m-tile 2*pm + r (128 rows) against all 256 columns. An
@@ -33,7 +41,8 @@ constexpr int kEpiWarps = 8;                             // 2 per TMEM lane quad
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBlockK * 2;          // 16 KB
 constexpr uint32_t kBBytes = (kBN / 2) * kBlockK * 2;    // 16 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 32 KB per k-block
+constexpr int kWideKB = 2;  // k-blocks per stage of the bf16 tile-loaded kernel
 constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 // Pair m-tiles per raster group: 16 when the experts average at least 16
 // pair m-tiles (4096 rows), so that a group stays within one expert's weights
@@ -94,12 +103,14 @@ template <bool kFp8, bool kQOut, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a,
                              const __grid_constant__ CUtensorMap tm_b, GemmArgs p) {
-  constexpr int kKE = kFp8 ? 128 : kBlockK;  // K elements per stage
+  constexpr int kKE = kFp8 ? 128 : kBlockK;  // K elements per k-block
+  constexpr int kKBS = kGather ? 1 : kWideKB;  // k-blocks per stage
+  constexpr uint32_t kSB = kKBS * kStageBytes;             // bytes per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int nst = p.stages;  // pipeline depth, chosen by the launcher to fit shared memory
   // FP8 column scales of the current tile, 128 per epilogue warp
-  float* col_scale = reinterpret_cast<float*>(smem + nst * kStageBytes);
+  float* col_scale = reinterpret_cast<float*>(smem + nst * kSB);
   uint64_t* full = reinterpret_cast<uint64_t*>(col_scale + (kFp8 ? kEpiWarps * (kBN / 2) : 0));
   uint64_t* empty = full + nst;
   uint64_t* tfull = empty + nst;
@@ -179,7 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_pm = pm_prefix[E];
   const int n_tiles_n = (p.N + kBN - 1) / kBN;
   const int total = total_pm * n_tiles_n;
-  const int nk = (p.K + kKE - 1) / kKE;  // a partial last block reads zeros past K
+  // stages per tile; a partial last stage reads zeros past K (A and B are
+  // bounded by K in their tensor maps)
+  const int nk = (p.K + kKE * kKBS - 1) / (kKE * kKBS);
   const WaitCtl wc{abort_flag, p.dev_status, p.timeout_ns};
   // A wait that gives up stops the peer CTA too: its waits see the raised
   // flag within a few polls, so the pair aborts together.
@@ -205,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_first = l2_policy_evict_first();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
         const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
-        const int b_row = c.e * p.K;
         const int b_col = c.n0 + static_cast<int>(rank) * (kBN / 2);
         const uint64_t pol_a =
             (p.a_hint == kAHintLastDemote && c.n0 / kBN == n_tiles_n - 1) ? pol_first : pol_last;
@@ -227,25 +239,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-          uint8_t* sa = smem + stage * kStageBytes;
-          uint8_t* sb = sa + kABytes;
+          uint8_t* sa = smem + stage * kSB;
+          uint8_t* sb = sa + kKBS * kABytes;
           if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kSB);
             // A rows are reused by every n-tile of the group
-            if constexpr (!kGather) {
-              if (p.a_hint == kAHintNormal)
-                tma_load_2d_pair(sa, &tm_a, bar, kb * kKE, c.row0);
-              else
-                tma_load_2d_pair_hint(sa, &tm_a, bar, kb * kKE, c.row0, pol_a);
-            }
             if constexpr (kFp8) {
-              // B^T [E*N, K] e4m3: this CTA's 128 output columns as K-major rows
-              tma_load_2d_pair(sb, &tm_b, bar, kb * kKE, c.e * p.N + b_col);
-            } else {
+              // A e4m3 [rows, K] and B^T [E*N, K] (this CTA's 128 output
+              // columns as K-major rows): one box per k-block, a k-block
+              // past K read as zeros
+              for (int r = 0; r < kKBS; ++r) {
+                const int k0 = (kb * kKBS + r) * kKE;
+                tma_load_2d_pair_hint(sa + r * kABytes, &tm_a, bar, k0, c.row0, pol_a);
+                tma_load_2d_pair(sb + r * kBBytes, &tm_b, bar, k0, c.e * p.N + b_col);
+              }
+            } else if constexpr (!kGather) {
+              // A: {64 k, 128 rows, kKBS k-blocks}
+              if (p.a_hint == kAHintNormal)
+                tma_load_3d_pair(sa, &tm_a, bar, 0, c.row0, kb * kKBS);
+              else
+                tma_load_3d_pair_hint(sa, &tm_a, bar, 0, c.row0, kb * kKBS, pol_a);
+            }
+            if constexpr (!kFp8) {
+              // B [E][K][N] as {64 columns, 64*kKBS k-rows, expert e}
 #pragma unroll
               for (int cb = 0; cb < kBN / 2 / 64; ++cb)
-                tma_load_2d_pair(sb + cb * (64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
-                                 b_row + kb * kBlockK);
+                tma_load_3d_pair(sb + cb * (kKBS * 64 * kBlockK * 2), &tm_b, bar, b_col + 64 * cb,
+                                 kb * kKBS * kBlockK, c.e);
             }
           }
           if constexpr (kGather)
@@ -285,9 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = max(0, hi - nst); i < hi; ++i) {
             uint64_t* b = &full[i % nst];
             if (i >= issued)
-              mbar_arrive_expect_tx(b, kStageBytes);  // armed here for the peer's half alone
+              mbar_arrive_expect_tx(b, kSB);  // armed here for the peer's half alone
             else if (i >= theirs)
-              mbar_complete_tx(b, kStageBytes);       // the peer's half will never come
+              mbar_complete_tx(b, kSB);       // the peer's half will never come
             mbar_wait_drain(b, static_cast<uint32_t>(i / nst) & 1u, kDrainLimitNs);
           }
         }
@@ -313,22 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * kStageBytes);
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t a_addr = smem_u32(smem + stage * kSB);
+          const uint32_t b_addr = a_addr + kKBS * kABytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // A: K-major 128-byte rows; one UMMA K step (16 bf16 or 32 e4m3)
-            // is 32 bytes.
-            const uint64_t ad = smem_desc_sw128(a_addr + 32u * kk, 16u, 1024u);
-            if constexpr (kFp8) {
-              // B: K-major like A
-              const uint64_t bd = smem_desc_sw128(b_addr + 32u * kk, 16u, 1024u);
-              umma_f8_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            } else {
-              // B: MN-major, one 128-byte row per k, 16-row K step = 2 KB,
-              // this CTA's two 64-column blocks 8 KB apart.
-              const uint64_t bd = smem_desc_sw128(b_addr + 2048u * kk, 64u * kBlockK * 2, 1024u);
-              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int r = 0; r < kKBS; ++r) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // A: K-major 128-byte rows, k-block r at r * 16 KB; one UMMA K
+              // step (16 bf16 or 32 e4m3) is 32 bytes.
+              const uint64_t ad = smem_desc_sw128(a_addr + kABytes * r + 32u * kk, 16u, 1024u);
+              const uint32_t acc_in = (kb | r | kk) != 0 ? 1u : 0u;
+              if constexpr (kFp8) {
+                // B: K-major like A
+                const uint64_t bd = smem_desc_sw128(b_addr + kBBytes * r + 32u * kk, 16u, 1024u);
+                umma_f8_pair(d_tmem, ad, bd, idesc, acc_in);
+              } else {
+                // B: MN-major, one 128-byte row per k (16-row K step = 2 KB,
+                // k-block r at r * 8 KB), this CTA's two 64-column blocks
+                // kKBS * 8 KB apart.
+                const uint64_t bd = smem_desc_sw128(b_addr + 8192u * r + 2048u * kk,
+                                                    kKBS * 64u * kBlockK * 2, 1024u);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, acc_in);
+              }
             }
           }
           umma_commit_pair_multicast(&empty[stage], 0x3);
@@ -500,8 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t gemm_pair_smem_bytes(int E, int stages, bool fp8) {
-  return 1024 + static_cast<size_t>(stages) * kStageBytes + (fp8 ? 4 * kEpiWarps * (kBN / 2) : 0) +
+size_t gemm_pair_smem_bytes(int E, int stages, bool fp8, int kb_per_stage) {
+  return 1024 + static_cast<size_t>(stages) * kStageBytes * kb_per_stage +
+         (fp8 ? 4 * kEpiWarps * (kBN / 2) : 0) +
          8 * (2 * stages + 6) + 16 + 8 * static_cast<size_t>(E + 1);
 }
 
@@ -515,10 +542,12 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
   GemmArgs args = a;
+  constexpr int kbs = kGather ? 1 : kWideKB;
   args.stages = kMaxStages;
-  while (args.stages > 2 && gemm_pair_smem_bytes(a.E, args.stages, kFp8) > static_cast<size_t>(optin))
+  while (args.stages > 2 &&
+         gemm_pair_smem_bytes(a.E, args.stages, kFp8, kbs) > static_cast<size_t>(optin))
     --args.stages;
-  const size_t smem = gemm_pair_smem_bytes(a.E, args.stages, kFp8);
+  const size_t smem = gemm_pair_smem_bytes(a.E, args.stages, kFp8, kbs);
   err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFp8, kQOut, kGather>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -193,7 +193,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tm_a, const CUtensorMap& tm_b
                                 const GemmArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_grouped_gemm_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                      const GemmArgs& a, int num_sms, cudaStream_t st);
-size_t gemm_pair_smem_bytes(int E, int stages, bool fp8);
+size_t gemm_pair_smem_bytes(int E, int stages, bool fp8, int kb_per_stage);
 // FP8 operands; writes D (bf16), or Dq + d_scale when a.Dq is set
 cudaError_t launch_grouped_gemm_pair_fp8(const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                          const GemmArgs& a, int num_sms, cudaStream_t st);
