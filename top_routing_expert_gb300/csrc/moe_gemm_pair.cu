@@ -57,6 +57,16 @@ struct PairTile {
   int e, row0, row_end, n0;
 };
 
+// n-tile index of pair tile L (the raster arithmetic of decode_pair).
+__device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_tiles_n,
+                                            int forced_group) {
+  const int group = raster_group(total_pm, E, forced_group);
+  const int per_group = group * n_tiles_n;
+  const int g = L / per_group;
+  const int gsz = min(group, total_pm - g * group);
+  return (L - g * per_group) / gsz;
+}
+
 __device__ __forceinline__ PairTile decode_pair(int L, const int* pm_prefix, const int* offs,
                                                 int E, int total_pm, int n_tiles_n, int rank,
                                                 int forced_group) {
@@ -218,7 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_first = l2_policy_evict_first();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
         const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
-        const int b_col = c.n0 + static_cast<int>(rank) * (kBN / 2);
+        // A last n-tile of at most 128 columns runs as an N = 128 UMMA, each
+        // CTA holding 64 of its columns (the loads stay the same size: the
+        // extra columns are read and never used).
+        const bool half_n = p.N - c.n0 <= kBN / 2;
+        const int b_col = c.n0 + static_cast<int>(rank) * (half_n ? kBN / 4 : kBN / 2);
         const uint64_t pol_a =
             (p.a_hint == kAHintLastDemote && c.n0 / kBN == n_tiles_n - 1) ? pol_first : pol_last;
         int gr[4] = {0, 0, 0, 0};
@@ -316,8 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------- UMMA issuer (leader) ----
-      const uint32_t idesc =
+      const uint32_t idesc_full =
           kFp8 ? idesc_e4m3_f32(2 * kBM, kBN) : idesc_bf16_f32(2 * kBM, kBN, false, true);
+      const uint32_t idesc_half = kFp8 ? idesc_e4m3_f32(2 * kBM, kBN / 2)
+                                       : idesc_bf16_f32(2 * kBM, kBN / 2, false, true);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -327,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pair_wait(&tempty[acc], acc_phase ^ 1u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        const int nt = pair_tile_nt(L, E, total_pm, n_tiles_n, p.group);
+        const uint32_t idesc = p.N - nt * kBN <= kBN / 2 ? idesc_half : idesc_full;
         for (int kb = 0; kb < nk; ++kb) {
           if (!pair_wait(&full[stage], phase)) {
             aborted = true;
