@@ -181,6 +181,13 @@ def _route_gpu(s, x, gate, bias):
     (300, 64, 256, 8, None),      # one K block, maximum E
     (700, 1024, 64, 6, None),
     (130, 4096, 128, 2, "normal"),  # long K, many experts
+    # stages hold 4, 2 or 1 k-blocks (the largest dividing H/64 that leaves
+    # two stages): three single-k-block stages; two-k-block stages with the
+    # gate read as given and its second 64-expert box mostly zero fill; and
+    # the persistent kernel (more 128-token tiles than SMs) with two
+    (1000, 192, 12, 3, None),
+    (700, 384, 72, 4, "normal"),
+    (20000, 384, 12, 2, None),
 ])
 def test_router_gemm_against_oracle(T, H, E, k, bias):
     gen = torch.Generator().manual_seed(T + H + E)
