@@ -255,16 +255,20 @@ bool tmap_bf16_kblocks(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t row
 }
 
 // Per-expert bf16 matrices W [E][K][N] (row-major, N % 64 == 0) seen as
-// 3-D {N, K, E}, read in boxes of 64 columns x box_k rows of one expert.
+// 4-D {64 columns, K, N/64 column blocks, E}, the column-block dimension
+// 128 bytes apart, read in boxes of box_k rows x 2 column blocks of one
+// expert: one copy fills a CTA's 128-column B slice, block by block (each
+// block the box_k x 128-byte swizzled tile a 2-D {64, box_k} box gives).
+// Rows past K and blocks past N read as zeros.
 bool tmap_bf16_experts(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t K, uint64_t E,
                        uint32_t box_k) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t gdim[3] = {N, K, E};
-  const cuuint64_t gstride[2] = {N * 2, N * K * 2};
-  const cuuint32_t box[3] = {64, box_k, 1};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
+  const cuuint64_t gdim[4] = {64, K, N / 64, E};
+  const cuuint64_t gstride[3] = {N * 2, 128, N * K * 2};
+  const cuuint32_t box[4] = {64, box_k, 2, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), gdim, gstride, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -439,8 +443,8 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
     return MOE_ERR_CUDA;
   }
   if (pair) {
-    // W [E][K][N] in boxes of 64 columns x 64 (gathered A) or 128 k-rows of one
-    // expert: rows past K read as zeros
+    // W [E][K][N] in boxes of 128 columns x 64 (gathered A) or 128 k-rows of
+    // one expert: rows past K read as zeros
     if (!tmap_bf16_experts(&tm_b, W, N, K, d.E, a_rows != nullptr ? kBlockK : 2 * kBlockK))
       return MOE_ERR_CUDA;
   } else if (!tmap_bf16_2d(&tm_b, W, N, static_cast<uint64_t>(d.E) * K, 64, kBlockK)) {

@@ -361,6 +361,18 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(void* smem_dst, const CUte
       : "memory");
 }
 
+// 4-D form of tma_load_2d_pair.
+__device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t mbar_cluster_addr, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
 // Four rows of a 2-D tensor (row indices r0..r3, one 128-byte box row each,
 // from column c0) into consecutive 128-byte rows at smem_dst; the map's box
 // is one row high. Transaction bytes counted as in tma_load_2d_pair.
