@@ -466,8 +466,6 @@ moe_status run_gemm(const Dims& d, const moe_bf16* A, const moe_bf16* W, const i
   g.a_rows = a_rows;
   g.a_src_rows = a_src_rows;
   g.stages = 0;
-  g.group = 0;
-  g.a_hint = kAHintLast;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   if (pair)
@@ -504,8 +502,6 @@ moe_status run_gemm_fp8(const Dims& d, const uint8_t* Aq, const float* a_scale,
   g.a_rows = nullptr;
   g.a_src_rows = 0;
   g.stages = 0;
-  g.group = 0;
-  g.a_hint = kAHintLast;
   g.dev_status = status;
   g.timeout_ns = wait_timeout_ns();
   MOE_CUDA(launch_grouped_gemm_pair_fp8(tm_a, tm_b, g, num_sms(), st));

@@ -48,8 +48,7 @@ constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 // pair m-tiles (4096 rows), so that a group stays within one expert's weights
 // (1.7 % faster on the power-capped large-expert layer, whose DRAM traffic it
 // lowers); 8 for smaller or ragged experts (0.5-0.8 % faster there).
-__device__ __forceinline__ int raster_group(int total_pm, int E, int forced) {
-  if (forced > 0) return forced;
+__device__ __forceinline__ int raster_group(int total_pm, int E) {
   return total_pm >= 16 * E ? 16 : 8;
 }
 
@@ -58,9 +57,8 @@ struct PairTile {
 };
 
 // n-tile index of pair tile L (the raster arithmetic of decode_pair).
-__device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_tiles_n,
-                                            int forced_group) {
-  const int group = raster_group(total_pm, E, forced_group);
+__device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_tiles_n) {
+  const int group = raster_group(total_pm, E);
   const int per_group = group * n_tiles_n;
   const int g = L / per_group;
   const int gsz = min(group, total_pm - g * group);
@@ -68,9 +66,8 @@ __device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_ti
 }
 
 __device__ __forceinline__ PairTile decode_pair(int L, const int* pm_prefix, const int* offs,
-                                                int E, int total_pm, int n_tiles_n, int rank,
-                                                int forced_group) {
-  const int group = raster_group(total_pm, E, forced_group);
+                                                int E, int total_pm, int n_tiles_n, int rank) {
+  const int group = raster_group(total_pm, E);
   const int per_group = group * n_tiles_n;
   const int g = L / per_group;
   const int first = g * group;
@@ -224,17 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool aborted = false;
-      const uint64_t pol_last = l2_policy_evict_last();
-      const uint64_t pol_first = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
-        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
+        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
         // A last n-tile of at most 128 columns runs as an N = 128 UMMA, each
         // CTA holding 64 of its columns (the loads stay the same size: the
         // extra columns are read and never used).
         const bool half_n = p.N - c.n0 <= kBN / 2;
         const int b_col = c.n0 + static_cast<int>(rank) * (half_n ? kBN / 4 : kBN / 2);
-        const uint64_t pol_a =
-            (p.a_hint == kAHintLastDemote && c.n0 / kBN == n_tiles_n - 1) ? pol_first : pol_last;
         int gr[4] = {0, 0, 0, 0};
         if constexpr (kGather) {
 #pragma unroll
@@ -257,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sb = sa + kKBS * kABytes;
           if (lane == 0) {
             if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kSB);
-            // A rows are reused by every n-tile of the group
+            // A rows are reused by every n-tile of the group: keep them in L2
             if constexpr (kFp8) {
               // A e4m3 [rows, K] and B^T [E*N, K] (this CTA's 128 output
               // columns as K-major rows): one box per k-block, a k-block
@@ -269,10 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else if constexpr (!kGather) {
               // A: {64 k, 128 rows, kKBS k-blocks}
-              if (p.a_hint == kAHintNormal)
-                tma_load_3d_pair(sa, &tm_a, bar, 0, c.row0, kb * kKBS);
-              else
-                tma_load_3d_pair_hint(sa, &tm_a, bar, 0, c.row0, kb * kKBS, pol_a);
+              tma_load_3d_pair_hint(sa, &tm_a, bar, 0, c.row0, kb * kKBS, pol_a);
             }
             if constexpr (!kFp8) {
               // B [E][K][N]: this CTA's two 64-column blocks x 64*kKBS k-rows
@@ -343,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pair_wait(&tempty[acc], acc_phase ^ 1u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        const int nt = pair_tile_nt(L, E, total_pm, n_tiles_n, p.group);
+        const int nt = pair_tile_nt(L, E, total_pm, n_tiles_n);
         const uint32_t idesc = p.N - nt * kBN <= kBN / 2 ? idesc_half : idesc_full;
         for (int kb = 0; kb < nk; ++kb) {
           if (!pair_wait(&full[stage], phase)) {
@@ -404,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = cluster; L < total; L += n_clusters) {
-      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, p.group);
+      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
       const int row = c.row0 + 32 * q + lane;
       const bool valid = row < c.row_end;
       const int col0 = c.n0 + half * (kBN / 2);

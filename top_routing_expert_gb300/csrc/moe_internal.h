@@ -115,17 +115,9 @@ struct GemmArgs {
   const int32_t* a_rows;   // optional: A row r is row a_rows[r] of the A tensor (a gather,
   int a_src_rows;          //   by TMA, from a tensor of a_src_rows rows); CTA-pair kernel
   int stages;              // CTA-pair kernel: pipeline depth (set by its launcher)
-  int group;               // CTA-pair kernel: pair m-tiles per raster group (0: by size)
-  int a_hint;              // CTA-pair kernel: L2 priority of A loads (kAHint* below)
   uint32_t* dev_status;
   uint64_t timeout_ns;
 };
-
-// L2 eviction priority the CTA-pair GEMM gives its A (row-panel) loads:
-// normal; evict-last (kept for the group's other n-tiles); or evict-last
-// except on the last n-tile of a group, whose loads mark the lines
-// evict-first again, so that finished groups do not keep L2 from later ones.
-enum { kAHintNormal = 0, kAHintLast = 1, kAHintLastDemote = 2 };
 
 // How the router's B operand (the gate, N = E_pad experts x K = H) reaches
 // each pipeline stage:

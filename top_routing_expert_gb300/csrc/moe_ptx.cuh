@@ -136,16 +136,10 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// L2 eviction-priority policies for TMA loads (createpolicy, whole range).
+// L2 eviction-priority policy for TMA loads (createpolicy, whole range).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
@@ -340,16 +334,7 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// 3-D forms of tma_load_2d_pair and tma_load_2d_pair_hint.
-__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map,
-                                                 uint32_t mbar_cluster_addr, int32_t c0,
-                                                 int32_t c1, int32_t c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
+// 3-D form of tma_load_2d_pair_hint.
 __device__ __forceinline__ void tma_load_3d_pair_hint(void* smem_dst, const CUtensorMap* map,
                                                       uint32_t mbar_cluster_addr, int32_t c0,
                                                       int32_t c1, int32_t c2, uint64_t policy) {
