@@ -723,7 +723,10 @@ def _uniforms(T, E, seed):
 
 
 @pytest.mark.parametrize("T,H,E,k,tau", [(1000, 512, 12, 3, 1.0), (777, 256, 64, 6, 0.5),
-                                         (300, 1024, 8, 2, 2.0), (5000, 256, 128, 2, 1.0)])
+                                         (300, 1024, 8, 2, 2.0), (5000, 256, 128, 2, 1.0),
+                                         # the persistent router (more 128-token tiles
+                                         # than SMs), noise written back to TMEM
+                                         (20000, 384, 72, 4, 0.7)])
 def test_route_gumbel_against_oracle(T, H, E, k, tau):
     gen = torch.Generator().manual_seed(T + E)
     x = torch.randn((T, H), generator=gen).to(torch.bfloat16)
