@@ -755,7 +755,9 @@ def test_route_gumbel_against_oracle(T, H, E, k, tau):
     mism = routing_flips(gidx, r.idx, topk_margins(z, k), f"gumbel router E={E}",
                          slack=1 + np.abs(z).max(), extra=gerr.max(axis=1))
     ok = np.setdiff1d(np.arange(T), mism)
-    assert np.abs(w.cpu().numpy()[ok] - r.w[ok]).max() <= 1e-5
+    # a weight is a softmax of the chosen scores: |dw| <= max_j |dz_j|
+    w_tol = 1e-5 + gerr.max(axis=1)[ok, None]
+    assert (np.abs(w.cpu().numpy()[ok] - r.w[ok]) <= w_tol).all()
     stt, _ = assert_dispatch_on_gpu_indices(gidx, r.p, E, 1, routed=routed.cpu().numpy(),
                                             aux=float(aux.item()), aux_rel=1e-4)
     assert np.allclose(P.cpu().numpy(), stt.P, rtol=1e-4, atol=1e-6)
