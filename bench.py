@@ -39,8 +39,8 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) per grouped-GEMM launch, averaged over GEMM1 and
 # GEMM2, from the ncu capture summarised in profiles/ (null until captured
 # for the current kernel).
-TRAFFIC = {"large_expert": 8.50e9}
-TRAFFIC_FP8 = {"large_expert": 4.52e9}
+TRAFFIC = {"large_expert": 8.54e9}
+TRAFFIC_FP8 = {"large_expert": 4.43e9}
 
 
 def launches_per_step(w: W.Workload, fp8: bool) -> int:
