@@ -188,6 +188,11 @@ def _route_gpu(s, x, gate, bias):
     (1000, 192, 12, 3, None),
     (700, 384, 72, 4, "normal"),
     (20000, 384, 12, 2, None),
+    # 256 experts (four 64-expert gate boxes per k-block): two k-blocks per
+    # stage in the per-tile kernel; one in the persistent kernel, where the
+    # top-8 epilogue scratch leaves room for no more
+    (400, 512, 256, 8, None),
+    (20000, 256, 256, 8, "normal"),
 ])
 def test_router_gemm_against_oracle(T, H, E, k, bias):
     gen = torch.Generator().manual_seed(T + H + E)
