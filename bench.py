@@ -39,7 +39,7 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM bytes (read + write) per grouped-GEMM launch, averaged over GEMM1 and
 # GEMM2, from the ncu capture summarised in profiles/ (null until captured
 # for the current kernel).
-TRAFFIC = {"large_expert": 8.54e9}
+TRAFFIC = {"large_expert": 7.92e9}
 TRAFFIC_FP8 = {"large_expert": 4.43e9}
 
 

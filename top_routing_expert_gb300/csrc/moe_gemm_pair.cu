@@ -45,11 +45,14 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 32 KB per k-block
 constexpr int kWideKB = 2;  // k-blocks per stage of the bf16 tile-loaded kernel
 constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 // Pair m-tiles per raster group: 16 when the experts average at least 16
-// pair m-tiles (4096 rows), so that a group stays within one expert's weights
-// (1.7 % faster on the power-capped large-expert layer, whose DRAM traffic it
-// lowers); 8 for smaller or ragged experts (0.5-0.8 % faster there).
-__device__ __forceinline__ int raster_group(int total_pm, int E) {
-  return total_pm >= 16 * E ? 16 : 8;
+// pair m-tiles (4096 rows) and A's rows are short, so that a group stays
+// within one expert's weights (1.7 % faster on the power-capped large-expert
+// layer, whose DRAM traffic it lowers); 8 for smaller or ragged experts
+// (0.5-0.8 % faster there) and for A rows of 16 KB or more, where a group's
+// A panels are 8 x 256 such rows (the large-expert bf16 GEMM2, K = 14336,
+// read 9.7 instead of 10.9 GB per launch, in the same time).
+__device__ __forceinline__ int raster_group(int total_pm, int E, int a_row_bytes) {
+  return (total_pm >= 16 * E && a_row_bytes < 16384) ? 16 : 8;
 }
 
 struct PairTile {
@@ -57,8 +60,9 @@ struct PairTile {
 };
 
 // n-tile index of pair tile L (the raster arithmetic of decode_pair).
-__device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_tiles_n) {
-  const int group = raster_group(total_pm, E);
+__device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_tiles_n,
+                                            int a_row_bytes) {
+  const int group = raster_group(total_pm, E, a_row_bytes);
   const int per_group = group * n_tiles_n;
   const int g = L / per_group;
   const int gsz = min(group, total_pm - g * group);
@@ -66,8 +70,9 @@ __device__ __forceinline__ int pair_tile_nt(int L, int E, int total_pm, int n_ti
 }
 
 __device__ __forceinline__ PairTile decode_pair(int L, const int* pm_prefix, const int* offs,
-                                                int E, int total_pm, int n_tiles_n, int rank) {
-  const int group = raster_group(total_pm, E);
+                                                int E, int total_pm, int n_tiles_n, int rank,
+                                                int a_row_bytes) {
+  const int group = raster_group(total_pm, E, a_row_bytes);
   const int per_group = group * n_tiles_n;
   const int g = L / per_group;
   const int first = g * group;
@@ -196,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_pm = pm_prefix[E];
   const int n_tiles_n = (p.N + kBN - 1) / kBN;
+  const int a_row_bytes = p.K * (kFp8 ? 1 : 2);
   const int total = total_pm * n_tiles_n;
   // stages per tile; a partial last stage reads zeros past K (A and B are
   // bounded by K in their tensor maps)
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool aborted = false;
       const uint64_t pol_a = l2_policy_evict_last();
       for (int L = cluster; L < total && !aborted; L += n_clusters) {
-        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+        const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, a_row_bytes);
         // A last n-tile of at most 128 columns runs as an N = 128 UMMA, each
         // CTA holding 64 of its columns (the loads stay the same size: the
         // extra columns are read and never used).
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!pair_wait(&tempty[acc], acc_phase ^ 1u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        const int nt = pair_tile_nt(L, E, total_pm, n_tiles_n);
+        const int nt = pair_tile_nt(L, E, total_pm, n_tiles_n, a_row_bytes);
         const uint32_t idesc = p.N - nt * kBN <= kBN / 2 ? idesc_half : idesc_full;
         for (int kb = 0; kb < nk; ++kb) {
           if (!pair_wait(&full[stage], phase)) {
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int L = cluster; L < total; L += n_clusters) {
-      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank);
+      const PairTile c = decode_pair(L, pm_prefix, offs, E, total_pm, n_tiles_n, rank, a_row_bytes);
       const int row = c.row0 + 32 * q + lane;
       const bool valid = row < c.row_end;
       const int col0 = c.n0 + half * (kBN / 2);
