@@ -64,7 +64,9 @@ import numpy as np
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact value of bf16 bit patterns (uint16) as float64."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
+    # a signalling-NaN pattern widens to a quiet NaN; that is its value here
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
 
 
 def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
